@@ -1,0 +1,385 @@
+// Forward kernel: exact softmax attention with the online softmax.
+//
+// "Interrogating the GPU part 5: FlashAttention", "How does tiling remove the
+// traffic?" (a query block stays on chip while key/value blocks stream past)
+// and "How can you softmax a row you never see whole?" (running max m,
+// running sum l, rescaled accumulator; O = o / l at the end); "LLM Flash
+// Attention", "End-to-end flow" (one write of O and of the per-row LSE;
+// causal block skipping).  Blackwell form of the parts named in
+// "Why did Blackwell need FlashAttention-4?": accumulators in tensor memory,
+// conditional rescaling.
+//
+// One CTA owns two query tiles of 128 rows (a "tile pair") of one (batch,
+// head).  Warp roles (320 threads):
+//   warps 0-3  softmax warpgroup of tile 0 (thread = query row)
+//   warps 4-7  softmax warpgroup of tile 1
+//   warp  8    MMA issuer (one thread) and TMEM owner
+//   warp  9    TMA producer (one thread)
+// Tensor memory (512 columns): S_t at column 128 t (128 fp32 columns; the
+// bf16 probabilities P_t overwrite its first 64 columns), O_t at 256 + d t.
+// Shared memory: Q_0, Q_1 and a ring of NSLOT K/V tiles, all 128 x d bf16
+// with 128-byte swizzle.
+//
+// Per key block j the MMA thread issues S_0 = Q_0 K_j^T, S_1 = Q_1 K_j^T, then,
+// as each softmax warpgroup publishes P_t, O_t += P_t V_j.  While warpgroup 0
+// exponentiates S_0 the tensor core works on tile 1 and vice versa.  Because
+// P_t lives in S_t's columns, S_t for block j+1 is issued only after the MMA
+// O_t += P_t V_j has completed.
+//
+// Scores are handled in base 2: the softmax works on s * scale * log2(e), so
+// each probability is one ex2; LSE is converted back to natural-log units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// Conditional rescale threshold (log2 units): the running maximum used as the
+// exponent reference is only moved when a block raises the row maximum by
+// more than this, so probabilities stay below 2^8 and most blocks skip the
+// correction of l and O.  Any value gives the same result in exact
+// arithmetic because l, O and the LSE all use the same reference.
+constexpr float kRescaleThresholdLog2 = 8.0f;
+
+constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;  // waits while draining after an abort
+
+template <int D>
+struct FwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kTileRows = 128;
+  static constexpr int kTileBytes = kTileRows * D * 2;
+  static constexpr int kAtoms = D / 64;  // 64-column atom columns per tile
+  static constexpr int kSlots = (D == 128) ? 4 : 8;
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSCol0 = 0, kSCol1 = 128;
+  static constexpr uint32_t kOCol0 = 256, kOCol1 = 256 + D;
+  static constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kSlots * kTileBytes + 256;
+};
+
+struct FwdBarriers {
+  uint64_t q_full;
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t drain;
+  uint64_t never;  // signalled by nothing: the debug stall waits on it
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct FwdParams {
+  __nv_bfloat16* o;
+  float* lse;
+  int N;
+  int num_pairs;
+  float scale_log2;  // scale * log2(e)
+  uint64_t wait_limit_ns;
+  int debug_stall;  // nonzero: the MMA thread first waits on `never` (tests the timeout path)
+};
+
+// wait sites reported in the status word
+enum : int { kSiteStall = 0, kSiteFwdProducer = 1, kSiteFwdQ, kSiteFwdK, kSiteFwdV, kSiteFwdPvDone, kSiteFwdP, kSiteFwdS, kSiteFwdO };
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + 2 * C::kTileBytes;
+  FwdBarriers* bar = reinterpret_cast<FwdBarriers*>(sKV + C::kSlots * C::kTileBytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int N = p.N;
+
+  // work item: pairs of a head are visited from the last (heaviest when causal) to the first
+  const int pr = blockIdx.x % p.num_pairs;
+  const int bh = blockIdx.x / p.num_pairs;
+  const int pair = p.num_pairs - 1 - pr;
+  const int q0 = pair * 256;
+  const bool has1 = q0 + 128 < N;
+  const int nblk = (N + 127) / 128;
+  const int nb0 = CAUSAL ? min(nblk, 2 * pair + 1) : nblk;
+  const int nb1 = has1 ? (CAUSAL ? min(nblk, 2 * pair + 2) : nblk) : 0;
+  const int nb_max = max(nb0, nb1);
+
+  if (tid == 0) {
+    mbar_init(&bar->q_full, 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(&bar->kv_full[s], 1);
+      mbar_init(&bar->kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar->s_full[t], 1);
+      mbar_init(&bar->p_full[t], 128);
+      mbar_init(&bar->pv_done[t], 1);
+    }
+    mbar_init(&bar->drain, 1);
+    mbar_init(&bar->never, 1);
+    bar->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(&bar->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 9 && lane == 0) {
+    tma_prefetch_map(&map_q);
+    tma_prefetch_map(&map_k);
+    tma_prefetch_map(&map_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar->tmem_base;
+  const WaitCtx ctx{&bar->abort_flag, p.wait_limit_ns};
+
+  if (warp == 9) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int fill = 0;
+      mbar_arrive_expect_tx(&bar->q_full, C::kTileBytes * (has1 ? 2 : 1));
+      for (int t = 0; t < (has1 ? 2 : 1); ++t)
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &map_q, &bar->q_full, a * 64, q0 + 128 * t, bh);
+      bool ok = true;
+      for (int j = 0; ok && j < nb_max; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int s = fill % C::kSlots;
+          const uint32_t u = fill / C::kSlots;
+          if (!wait_bounded(&bar->kv_empty[s], (u & 1) ^ 1, ctx, kSiteFwdProducer)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar->kv_full[s], C::kTileBytes);
+          const CUtensorMap* map = kv ? &map_v : &map_k;
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_3d(sKV + s * C::kTileBytes + a * 16384, map, &bar->kv_full[s], a * 64, j * 128, bh);
+          ++fill;
+        }
+      }
+      // every copy this thread started must land before the CTA can exit
+      wait_drain(&bar->q_full, 0, kDrainLimitNs);
+      for (int s = 0; s < C::kSlots; ++s) {
+        if (fill > s) {
+          const int uses = (fill - 1 - s) / C::kSlots + 1;
+          wait_drain(&bar->kv_full[s], (uses - 1) & 1, kDrainLimitNs);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 8) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
+      const uint64_t qdesc0 = sdesc_sw128(sq, 16, 1024);
+      const uint64_t qdesc1 = sdesc_sw128(sq + C::kTileBytes, 16, 1024);
+      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
+      int cons = 0;
+      bool ok = !(p.debug_stall && !wait_bounded(&bar->never, 0, ctx, kSiteStall));
+      ok = ok && wait_bounded(&bar->q_full, 0, ctx, kSiteFwdQ);
+      for (int j = 0; ok && j < nb_max; ++j) {
+        // ---- S_t = Q_t K_j^T
+        int s = cons % C::kSlots;
+        if (!wait_bounded(&bar->kv_full[s], (cons / C::kSlots) & 1, ctx, kSiteFwdK)) break;
+        tc_fence_after();
+        const uint64_t kdesc = sdesc_sw128(skv + s * C::kTileBytes, 16, 1024);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j < (t ? nb1 : nb0)) {
+            if (j > 0) {
+              if (!wait_bounded(&bar->pv_done[t], (j - 1) & 1, ctx, kSiteFwdPvDone)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint64_t qd = t ? qdesc1 : qdesc0;
+            const uint32_t dcol = tmem + (t ? C::kSCol1 : C::kSCol0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+              mma_bf16_ss(dcol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bar->s_full[t]);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bar->kv_empty[s]);
+        ++cons;
+        // ---- O_t += P_t V_j
+        s = cons % C::kSlots;
+        if (!wait_bounded(&bar->kv_full[s], (cons / C::kSlots) & 1, ctx, kSiteFwdV)) break;
+        tc_fence_after();
+        const uint64_t vdesc = sdesc_sw128(skv + s * C::kTileBytes, 16384, 1024);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j < (t ? nb1 : nb0)) {
+            if (!wait_bounded(&bar->p_full[t], j & 1, ctx, kSiteFwdP)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t dcol = tmem + (t ? C::kOCol1 : C::kOCol0);
+            const uint32_t pcol = tmem + (t ? C::kSCol1 : C::kSCol0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 2048) >> 4), id_pv,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bar->pv_done[t]);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bar->kv_empty[s]);
+        ++cons;
+      }
+      // everything issued must complete before the tensor memory is released
+      mma_commit(&bar->drain);
+      wait_drain(&bar->drain, 0, kDrainLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int nb = t ? nb1 : nb0;
+    const int row_g = q0 + 128 * t + r;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + (t ? C::kSCol1 : C::kSCol0) + lane_off;
+    const uint32_t tO = tmem + (t ? C::kOCol1 : C::kOCol0) + lane_off;
+    const float sl2 = p.scale_log2;
+    float m = -CUDART_INF_F;  // exponent reference (log2 units), a stale running max
+    float l = 0.f, l_mma = 0.f;
+    bool alive = nb > 0;
+    for (int j = 0; alive && j < nb; ++j) {
+      if (!__all_sync(0xffffffffu, wait_bounded(&bar->s_full[t], j & 1, ctx, kSiteFwdS))) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
+
+      const int kbase = j * 128;
+      const bool tail = kbase + 128 > N;
+      const bool diag = CAUSAL && (kbase + 127 > q0 + 128 * t);
+      if (tail || diag) {
+        const int last = (CAUSAL ? min(N - 1, row_g) : N - 1) - kbase;  // last visible key of this row
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > last) sr[c >> 5][c & 31] = __float_as_uint(-CUDART_INF_F);
+      }
+      float mx = __uint_as_float(sr[0][0]);
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
+      const float m_new = fmaxf(m, mx * sl2);
+      // conditional rescale: move the exponent reference only when the row
+      // maximum rose by more than the threshold (always on the first block)
+      float alpha = 1.f;
+      bool rescale_warp = false;
+      if (j == 0) {
+        m = m_new;
+      } else {
+        const bool need = (m_new - m) > kRescaleThresholdLog2;
+        rescale_warp = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = ex2_approx(m - m_new);
+          m = m_new;
+        }
+      }
+      // p = 2^(s c - m) two at a time (packed fp32x2 FMA/adds).  Two row sums
+      // are kept: `l` of the fp32 probabilities (for the LSE) and `l_mma` of
+      // the bf16-rounded probabilities that the P V product actually uses (for
+      // the normalisation of O, so a dominant probability's rounding cancels).
+      const float2 c2 = make_float2(sl2, sl2);
+      const float2 mneg2 = make_float2(-m, -m);
+      float2 acc = make_float2(0.f, 0.f), acc_mma = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
+                                      c2, mneg2);
+          const float p0 = ex2_approx(x.x);
+          const float p1 = ex2_approx(x.y);
+          pk[i] = pack_bf16x2(p0, p1);
+          acc = __fadd2_rn(acc, make_float2(p0, p1));
+          acc_mma = __fadd2_rn(acc_mma, make_float2(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xffff0000u)));
+        }
+        tmem_st16(tS + 16 * c, pk);
+      }
+      l = l * alpha + (acc.x + acc.y);
+      l_mma = l_mma * alpha + (acc_mma.x + acc_mma.y);
+      if (rescale_warp) {
+        // O_t accumulated through block j-1 is complete (the commit behind
+        // s_full covers it) and the next P V waits for p_full, so the
+        // correction O <- alpha O can be applied in place here.
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tO + 32 * c, ov);
+          tmem_wait_ld();
+          reg_fence32(ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(tO + 32 * c, ov);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar->p_full[t]);
+    }
+    // epilogue: O = o / l, LSE = (m + log2 l) ln 2
+    if (alive) {
+      if (__all_sync(0xffffffffu, wait_bounded(&bar->pv_done[t], (nb - 1) & 1, ctx, kSiteFwdO))) {
+        tc_fence_after();
+        const float inv_l = 1.f / l_mma;
+        __nv_bfloat16* orow = p.o + ((size_t)bh * N + row_g) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tO + 32 * c, ov);
+          tmem_wait_ld();
+          reg_fence32(ov);
+          if (row_g < N) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(ov[8 * v4 + 0]) * inv_l, __uint_as_float(ov[8 * v4 + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * inv_l, __uint_as_float(ov[8 * v4 + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * inv_l, __uint_as_float(ov[8 * v4 + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * inv_l, __uint_as_float(ov[8 * v4 + 7]) * inv_l);
+              dst[v4] = w;
+            }
+          }
+        }
+        if (row_g < N) p.lse[(size_t)bh * N + row_g] = (m + log2f(l)) * 0.6931471805599453f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,238 @@
+// C-ABI entry points of the exact tiled attention library (declared in fa.h).
+//
+// Host side only: argument validation, TMA tensor-map encoding and kernel
+// launches.  All kernels live in the headers included below and are compiled
+// into this one translation unit, which keeps the device status word a
+// single per-device variable.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "fa.h"
+#include "sm103_ptx.cuh"
+#include "fa_fwd.cuh"
+#include "fa_bwd.cuh"
+
+namespace {
+
+std::atomic<unsigned long long> g_wait_limit_ns{0};
+std::atomic<int> g_debug_stall{0};
+constexpr unsigned long long kDefaultWaitLimitNs = 2000ull * 1000 * 1000;
+
+unsigned long long wait_limit_ns() {
+  const unsigned long long v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return v ? v : kDefaultWaitLimitNs;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// [B*H][N][d] bf16 viewed as a 3-D tensor (d, N, B*H); boxes of 64 x 128 rows,
+// 128-byte swizzle.  Rows past N inside a head read as zero.
+bool encode_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// shape checks shared by every entry point
+fa_status check_shape(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = (long long)B * H;
+  if (bh > 65535LL * 65535LL) return FA_ERR_INVALID_ARG;
+  if (bh * N * d >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+fa_status check_scale(float scale, int causal) {
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+template <typename Kernel>
+cudaError_t set_smem(Kernel kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int D, bool CAUSAL>
+fa_status launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const fa::FwdParams& p,
+                     int BH, cudaStream_t stream) {
+  using C = fa::FwdCfg<D>;
+  auto kernel = fa::fa_fwd_kernel<D, CAUSAL>;
+  if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
+  const long long grid = (long long)p.num_pairs * BH;
+  kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int D, bool CAUSAL>
+fa_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
+                     const fa::BwdParams& p, int BH, cudaStream_t stream) {
+  using C = fa::BwdCfg<D>;
+  auto kernel = fa::fa_bwd_kernel<D, CAUSAL>;
+  if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
+  const long long grid = (long long)p.nkb * BH;
+  kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status launch_preprocess(const void* o, const void* dout, float* delta, float* dq_acc, long long rows, int d,
+                            cudaStream_t stream) {
+  const long long per_block = 256 / (d / 8);
+  long long blocks = (rows + per_block - 1) / per_block;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  if (d == 128)
+    fa::fa_bwd_preprocess_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta, dq_acc, rows);
+  else
+    fa::fa_bwd_preprocess_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta, dq_acc, rows);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+void fa_set_wait_limit_ns(unsigned long long limit_ns) { g_wait_limit_ns.store(limit_ns); }
+
+void fa_debug_stall(int enable) { g_debug_stall.store(enable ? 1 : 0); }
+
+fa_status fa_check_device_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, fa::g_fa_device_status, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(fa::g_fa_device_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    return static_cast<fa_status>(word & 0xffu);
+  }
+  return FA_OK;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa_status st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale, causal)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  if (!encode_bhnd(&mq, q, BH, N, d) || !encode_bhnd(&mk, k, BH, N, d) || !encode_bhnd(&mv, v, BH, N, d))
+    return FA_ERR_CUDA;
+  fa::FwdParams p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.N = N;
+  p.num_pairs = (N + 255) / 256;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = wait_limit_ns();
+  p.debug_stall = g_debug_stall.load();
+  if (d == 128) return causal ? launch_fwd<128, true>(mq, mk, mv, p, BH, stream) : launch_fwd<128, false>(mq, mk, mv, p, BH, stream);
+  return causal ? launch_fwd<64, true>(mq, mk, mv, p, BH, stream) : launch_fwd<64, false>(mq, mk, mv, p, BH, stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d) != FA_OK) return 0;
+  const size_t rows = (size_t)B * H * N;
+  const size_t dq_bytes = (rows * d * sizeof(float) + 255) & ~size_t(255);
+  return dq_bytes + rows * sizeof(float);
+}
+
+fa_status fa_bwd_preprocess(const void* o, const void* dout, float* delta, int B, int H, int N, int d,
+                            cudaStream_t stream) {
+  if (!o || !dout || !delta) return FA_ERR_INVALID_ARG;
+  fa_status st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(delta)) return FA_ERR_MISALIGNED;
+  return launch_preprocess(o, dout, delta, nullptr, (long long)B * H * N, d, stream);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
+                 float scale, int causal, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+  fa_status st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale, causal)) != FA_OK) return st;
+  if (ws_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return FA_ERR_MISALIGNED;
+  const int BH = B * H;
+  const long long rows = (long long)BH * N;
+  float* dq_acc = static_cast<float*>(workspace);
+  const size_t dq_bytes = ((size_t)rows * d * sizeof(float) + 255) & ~size_t(255);
+  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + dq_bytes);
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_bhnd(&mq, q, BH, N, d) || !encode_bhnd(&mk, k, BH, N, d) || !encode_bhnd(&mv, v, BH, N, d) ||
+      !encode_bhnd(&mdo, dout, BH, N, d))
+    return FA_ERR_CUDA;
+  // 1. delta = rowsum(dO o O), dQ accumulator = 0
+  if ((st = launch_preprocess(o, dout, delta, dq_acc, rows, d, stream)) != FA_OK) return st;
+  // 2. dK, dV and the fp32 dQ accumulation
+  fa::BwdParams p;
+  p.lse = lse;
+  p.delta = delta;
+  p.dq_acc = dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.N = N;
+  p.nkb = (N + 127) / 128;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale = scale;
+  p.wait_limit_ns = wait_limit_ns();
+  p.debug_stall = g_debug_stall.load();
+  if (d == 128)
+    st = causal ? launch_bwd<128, true>(mq, mk, mv, mdo, p, BH, stream) : launch_bwd<128, false>(mq, mk, mv, mdo, p, BH, stream);
+  else
+    st = causal ? launch_bwd<64, true>(mq, mk, mv, mdo, p, BH, stream) : launch_bwd<64, false>(mq, mk, mv, mdo, p, BH, stream);
+  if (st != FA_OK) return st;
+  // 3. dQ = scale * dQ_acc -> bf16
+  const long long n8 = rows * d / 8;
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  fa::fa_dq_convert_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), scale, n8);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,186 @@
+"""Thin Python binding of the C ABI in ``include/fa.h`` (ctypes).
+
+Every function here has the name of the C entry point it wraps and does
+argument marshalling only: it checks dtypes, shapes, contiguity and devices of
+the torch tensors it is given, passes their device pointers and sizes to the
+library, and raises ``FaError`` on a non-OK status.  All arithmetic runs in the
+library's CUDA kernels; there is no other implementation behind these names.
+If the compiled library is missing, loading fails loudly.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_MISALIGNED = 2
+FA_ERR_UNSUPPORTED = 3
+FA_ERR_CUDA = 4
+FA_ERR_TIMEOUT = 5
+
+_STATUS_NAMES = {
+    FA_OK: "FA_OK",
+    FA_ERR_INVALID_ARG: "FA_ERR_INVALID_ARG",
+    FA_ERR_MISALIGNED: "FA_ERR_MISALIGNED",
+    FA_ERR_UNSUPPORTED: "FA_ERR_UNSUPPORTED",
+    FA_ERR_CUDA: "FA_ERR_CUDA",
+    FA_ERR_TIMEOUT: "FA_ERR_TIMEOUT",
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libfa.so (built by ``build.build_library``); raises if it is absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libfa.so not found at {p}: run __graft_entry__.build() (no fallback exists)")
+    lib = ctypes.CDLL(p)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp]
+    lib.fa_bwd_preprocess.restype = i
+    lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+    lib.fa_bwd_workspace_bytes.restype = sz
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_check_device_status.argtypes = [vp]
+    lib.fa_check_device_status.restype = i
+    lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.fa_set_wait_limit_ns.restype = None
+    lib.fa_debug_stall.argtypes = [i]
+    lib.fa_debug_stall.restype = None
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _shape4(t: torch.Tensor, name: str):
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be [B, H, N, d], got {tuple(t.shape)}")
+    return tuple(t.shape)
+
+
+def _check(t: torch.Tensor, name: str, dtype, shape, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+def _raise(status: int, where: str):
+    if status != FA_OK:
+        raise FaError(status, where)
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def fa_set_wait_limit_ns(limit_ns: int) -> None:
+    load_library().fa_set_wait_limit_ns(int(limit_ns))
+
+
+def fa_debug_stall(enable: bool) -> None:
+    """Test hook: kernels launched while enabled stall on a barrier nothing signals."""
+    load_library().fa_debug_stall(int(bool(enable)))
+
+
+def fa_check_device_status(stream=None) -> int:
+    """Synchronize the stream; return (and clear) the device status word."""
+    return int(load_library().fa_check_device_status(_stream_handle(stream)))
+
+
+def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None) -> None:
+    """O and LSE of softmax(scale Q K^T) V; tensors [B,H,N,d] bf16 and [B,H,N] fp32."""
+    B, H, N, d = _shape4(q, "q")
+    dev = q.device
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _check(t, name, torch.bfloat16, (B, H, N, d), dev)
+    _check(lse, "lse", torch.float32, (B, H, N), dev)
+    st = load_library().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               B, H, N, d, float(scale), int(bool(causal)), _stream_handle(stream))
+    _raise(st, "fa_fwd")
+
+
+def fa_bwd_preprocess(o, dout, delta, stream=None) -> None:
+    """delta = rowsum(dO * O) in fp32, [B,H,N]."""
+    B, H, N, d = _shape4(o, "o")
+    dev = o.device
+    _check(o, "o", torch.bfloat16, (B, H, N, d), dev)
+    _check(dout, "dout", torch.bfloat16, (B, H, N, d), dev)
+    _check(delta, "delta", torch.float32, (B, H, N), dev)
+    st = load_library().fa_bwd_preprocess(o.data_ptr(), dout.data_ptr(), delta.data_ptr(), B, H, N, d,
+                                          _stream_handle(stream))
+    _raise(st, "fa_bwd_preprocess")
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: bool, stream=None) -> None:
+    """dQ, dK, dV of attention by recomputation; workspace is a uint8 device tensor."""
+    B, H, N, d = _shape4(q, "q")
+    dev = q.device
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, name, torch.bfloat16, (B, H, N, d), dev)
+    _check(lse, "lse", torch.float32, (B, H, N), dev)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = load_library().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                               lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                               ws_bytes, B, H, N, d, float(scale), int(bool(causal)), _stream_handle(stream))
+    _raise(st, "fa_bwd")
+
+
+# ---------------------------------------------------------------------------
+# conveniences that allocate the outputs with torch and call the entry points
+# ---------------------------------------------------------------------------
+def attention_forward(q, k, v, scale: float, causal: bool = False, stream=None):
+    B, H, N, d = _shape4(q, "q")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, scale, causal, stream)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, dout, lse, scale: float, causal: bool = False, workspace=None, stream=None):
+    B, H, N, d = _shape4(q, "q")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
+    fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, stream)
+    return dq, dk, dv

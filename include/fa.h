@@ -1,0 +1,155 @@
+/*
+ * fa.h - C ABI of the exact tiled attention library for GB300 (sm_103a).
+ *
+ * The library computes exact softmax attention, O = softmax(scale * Q K^T) V,
+ * without ever writing an N x N matrix to device memory:
+ *
+ *   - the forward pass keeps a block of 128 queries on chip and streams the
+ *     keys and values past it in blocks of 128 with the online softmax
+ *     (running maximum m, running sum l = sum e^{s-m}, rescaled output
+ *     accumulator), then writes O and one log-sum-exp L_i = m_i + log l_i per
+ *     query row ("Interrogating the GPU part 5: FlashAttention", sections
+ *     "How does tiling remove the traffic?" and "How can you softmax a row you
+ *     never see whole?", online-softmax update equation; "LLM Flash
+ *     Attention", section "End-to-end flow");
+ *   - the backward pass recomputes every probability tile as
+ *     P_ij = exp(S_ij - L_i) from Q, K and the saved L, and forms
+ *     dV = P^T dO, dS = P o (dP - delta), dQ = scale dS K, dK = scale dS^T Q
+ *     ("Interrogating the GPU part 5: FlashAttention", section "What does the
+ *     backward pass do without P?", LSE equation and recompute formula).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout.  Q, K, V, O, dO, dQ, dK, dV are contiguous bf16 arrays laid out
+ *   [B][H][N][d] (row-major, d fastest).  LSE and delta are contiguous fp32
+ *   arrays [B][H][N].  Queries and keys share the length N.
+ * Scores.  S = scale * Q K^T; LSE is in natural-log units of the scaled scores.
+ * Causal.  causal = 1 hides key j from query i when j > i (top-left aligned);
+ *   causal = 0 attends to all N keys.
+ * Memory.  Every pointer is device memory owned by the caller; the library
+ *   allocates nothing (no cudaMalloc; tensor memory is taken and released
+ *   inside each thread block).  Its only state is one device status word per
+ *   device, used to report a kernel that gave up waiting (FA_ERR_TIMEOUT).
+ * Streams.  Calls only enqueue work on `stream` (0 = legacy default stream) and
+ *   return the launch status; they do not synchronize.  A device-side timeout
+ *   is reported later by fa_check_device_status.
+ * Errors.  Arguments are validated before anything is enqueued; on an error
+ *   nothing runs and no output is written.  Invalid sizes, a null pointer or
+ *   a non-finite / non-positive scale give FA_ERR_INVALID_ARG; a pointer not
+ *   on a 16-byte boundary gives FA_ERR_MISALIGNED; a head dimension other
+ *   than 64 or 128 gives FA_ERR_UNSUPPORTED; a failed CUDA call (including a
+ *   device without sm_103a support) gives FA_ERR_CUDA.
+ * Limits.  1 <= B, H, N; B * H * N * d < 2^31; B * H <= 65535 * 65535.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,
+  FA_ERR_MISALIGNED = 2,
+  FA_ERR_UNSUPPORTED = 3,
+  FA_ERR_CUDA = 4,
+  FA_ERR_TIMEOUT = 5
+} fa_status;
+
+/*
+ * Forward pass.  "Interrogating the GPU part 5: FlashAttention", sections
+ * "How does tiling remove the traffic?" and "How can you softmax a row you
+ * never see whole?" (online-softmax update equation), with the log-sum-exp
+ * of section "What does the backward pass do without P?"; causal block
+ * skipping as in "LLM Flash Attention", section "End-to-end flow".
+ *
+ *   q, k, v  in:  bf16 [B][H][N][d]
+ *   o        out: bf16 [B][H][N][d], O = softmax(scale Q K^T) V
+ *   lse      out: fp32 [B][H][N],   L_i = log sum_j exp(scale q_i . k_j)
+ *   scale    finite, > 0 (1/sqrt(d) for standard attention)
+ *   causal   0 or 1
+ *   d        64 or 128
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, cudaStream_t stream);
+
+/*
+ * Backward preprocess: delta_i = sum_c dO_ic * O_ic, one fp32 per query row.
+ * The term delta of dS = P o (dP - delta) in "Interrogating the GPU part 5:
+ * FlashAttention", section "What does the backward pass do without P?"; the
+ * pages do not define it, and the row sum of dO o O is its exact value
+ * (sum_j P_ij dP_ij with dP = dO V^T and O = P V).
+ *
+ *   o, dout  in:  bf16 [B][H][N][d]
+ *   delta    out: fp32 [B][H][N]
+ */
+fa_status fa_bwd_preprocess(const void* o, const void* dout, float* delta, int B, int H, int N, int d,
+                            cudaStream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator
+ * [B][H][N][d] followed (at a 256-byte boundary) by delta [B][H][N].
+ * Returns 0 for sizes fa_bwd would reject.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass by recomputation.  "Interrogating the GPU part 5:
+ * FlashAttention", section "What does the backward pass do without P?" (LSE
+ * equation, recompute formula P_ij = exp(S_ij - L_i), dV = P^T dO,
+ * dS = P o (dP - delta)); "LLM Flash Attention", section "End-to-end flow"
+ * (backward paragraph).  dQ is accumulated in fp32 in the workspace and cast
+ * to bf16 at the end.
+ *
+ *   q, k, v, o, dout  in:  bf16 [B][H][N][d]; o and lse as written by fa_fwd
+ *   lse               in:  fp32 [B][H][N]
+ *   dq, dk, dv        out: bf16 [B][H][N][d] (overwritten, not accumulated)
+ *   workspace         device scratch of ws_bytes >= fa_bwd_workspace_bytes(),
+ *                     16-byte aligned; its contents on entry are ignored
+ *   scale, causal     as passed to fa_fwd
+ * ws_bytes too small gives FA_ERR_INVALID_ARG.  dQ is summed with fp32
+ * atomics, so it is not bitwise repeatable from run to run.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
+                 float scale, int causal, cudaStream_t stream);
+
+/*
+ * Synchronizes `stream`, then returns and clears the current device's status
+ * word: FA_OK, or FA_ERR_TIMEOUT if a kernel of this library gave up waiting
+ * on one of its barriers since the last check (its outputs are then
+ * undefined), or FA_ERR_CUDA if the synchronization itself failed.
+ */
+fa_status fa_check_device_status(cudaStream_t stream);
+
+/*
+ * Upper bound, in nanoseconds, on every barrier wait inside the kernels
+ * launched after this call (process-wide; 0 restores the default of two
+ * seconds).  A wait that runs out makes the kernel stop early and report
+ * FA_ERR_TIMEOUT through fa_check_device_status; it never traps.  Meant for
+ * tests of that path.
+ */
+void fa_set_wait_limit_ns(unsigned long long limit_ns);
+
+/*
+ * Test hook for the timeout path.  While `enable` is nonzero, every kernel
+ * launched by fa_fwd / fa_bwd first makes its MMA-issuing thread wait on a
+ * barrier that nothing ever signals; that wait runs out after the wait limit
+ * (fa_set_wait_limit_ns), the kernel reports FA_ERR_TIMEOUT, drains the copies
+ * it started and returns without writing its outputs.  Process-wide; 0 (the
+ * default) turns it off.  Nothing traps or hangs.
+ */
+void fa_debug_stall(int enable);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */
