@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact tiled attention hot path on GB300.
+
+One step = one forward (fa_fwd) and one backward (fa_bwd: preprocess, main
+kernel, dQ cast) over the whole workload, inputs resident in device memory.
+Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host cores
+
+FLOPs are counted as 4 N^2 d per (batch, head) for the forward, halved when
+causal, and 2.5x that for the backward (five N x N x d products).
+Between timed steps the L2 cache is flushed by writing a 256 MiB buffer
+(outside the per-step CUDA events).  N > 1 (torchrun) runs one independent
+copy of the workload per GPU (weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from exact_tiled_attention_08_gb300.workloads import WORKLOADS, make_inputs, to_f32_numpy  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s at d=128 BF16 and % of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "b4_h16_n2048_d128"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = ["fa_fwd.cuh", "fa_bwd.cuh", "sm103_ptx.cuh", "fa_lib.cu"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "exact_tiled_attention_08_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when there is none for this workload or the kernel sources changed since."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    e = d.get(kernel, {}).get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def sample_flops(w, rows: int) -> float:
+    """Algorithmic fwd+bwd FLOPs of the first `rows` query rows of one head."""
+    pairs = rows * (rows + 1) / 2 if w.causal else rows * w.N
+    if w.causal and rows == w.N:
+        pairs = w.N * w.N / 2
+    return 4.0 * w.d * pairs * 3.5
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.device = device_index
+
+    def start(self):
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.device).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            sel = str(self.device)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", sel], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timings (the reference arm and the cpu_baseline leg)
+# ---------------------------------------------------------------------------
+def oracle_step(inp_np, w, b, h, rows):
+    from oracle import attention_bwd_ref, attention_fwd_ref
+
+    q, k, v, do = (inp_np[x][b, h] for x in ("q", "k", "v", "do"))
+    attention_fwd_ref(q[:rows], k, v, w.scale, w.causal)
+    attention_bwd_ref(q[:rows], k, v, do[:rows], w.scale, w.causal)
+
+
+def oracle_rows_for_budget(inp_np, w, seconds_per_step: float) -> int:
+    """Largest number of leading query rows of one head whose fwd+bwd oracle
+    fits the per-step budget (measured on a probe of 128 rows)."""
+    probe = min(128, w.N)
+    t0 = time.perf_counter()
+    oracle_step(inp_np, w, 0, 0, probe)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    per_row = dt / probe
+    rows = int(seconds_per_step / per_row)
+    return max(1, min(w.N, rows))
+
+
+def cpu_inputs(w, seed_offset=0):
+    inp = make_inputs(w.B, w.H, w.N, w.d, w.seed + seed_offset, w.key_outliers)
+    return inp, {x: to_f32_numpy(t) for x, t in inp.items()}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    _, inp_np = cpu_inputs(w)
+    total = args.steps + args.warmup
+    rows = oracle_rows_for_budget(inp_np, w, seconds_per_step=min(2.0, 150.0 / max(total, 1)))
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    for i in range(args.warmup):
+        oracle_step(inp_np, w, *heads[i % len(heads)], rows)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(inp_np, w, *heads[i % len(heads)], rows)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = sample_flops(w, rows) / (ms / 1e3) / 1e12
+    sample = f"per step: fwd+bwd of the first {rows} of {w.N} query rows of one (batch, head), cycling over heads"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, inp_np, budget_s: float):
+    rows = oracle_rows_for_budget(inp_np, w, seconds_per_step=min(budget_s / 3, 4.0))
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    done, flops = 0, 0.0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and done < len(heads):
+        oracle_step(inp_np, w, *heads[done], rows)
+        flops += sample_flops(w, rows)
+        done += 1
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"fwd+bwd of the first {rows} of {w.N} query rows of {done} of {len(heads)} heads "
+                      f"({dt:.1f} s, fp64 numpy)"}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local):
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device; the GPU arm has no CPU fallback")
+    from exact_tiled_attention_08_gb300 import fa
+    from exact_tiled_attention_08_gb300.build import build_library
+
+    build_library()
+    fa.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    scale = w.scale
+    inp_cpu, inp_np = cpu_inputs(w, seed_offset=7919 * rank)
+    q, k, v, do = (inp_cpu[x].to(dev) for x in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    fwd_flops, bwd_flops = w.fwd_flops(), w.bwd_flops()
+    step_flops = fwd_flops + bwd_flops
+
+    def step():
+        fa.fa_fwd(q, k, v, o, lse, scale, w.causal, stream)
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, w.causal, stream)
+
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            flush.zero_()
+            step()
+        st = fa.fa_check_device_status(stream)
+        if st != fa.FA_OK:
+            raise SystemExit(f"bench.py: device status {fa.fa_status_string(st)} after warm-up")
+        if not (torch.isfinite(o.float()).all() and torch.isfinite(dq.float()).all()):
+            raise SystemExit("bench.py: non-finite outputs after warm-up")
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+        for e in ev:
+            for x in e:
+                x.record(stream)  # creates the event so its handle can be passed to the library
+        torch.cuda.synchronize(dev)
+        clocks = ClockSampler(local)
+        clocks.start()
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        for i in range(K):
+            flush.zero_()
+            e = ev[i]
+            fa.fa_set_timing_events(e[2], e[3], e[4], e[5])
+            e[0].record(stream)
+            step()
+            e[1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        clock_info = clocks.stop()
+        fa.fa_set_timing_events()
+        st = fa.fa_check_device_status(stream)
+        if st != fa.FA_OK:
+            raise SystemExit(f"bench.py: device status {fa.fa_status_string(st)} in the timed region")
+    step_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    fwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    bwd_ms = statistics.mean(e[4].elapsed_time(e[5]) for e in ev)
+    step_ms_max = max_over_ranks(step_ms, world)
+    value = world * step_flops / (step_ms_max / 1e3) / 1e12
+
+    # ---- end to end through the C ABI with pinned host buffers
+    h_in = {x: inp_cpu[x].pin_memory() for x in ("q", "k", "v", "do")}
+    h_out = {"o": torch.empty_like(o, device="cpu").pin_memory(), "lse": torch.empty_like(lse, device="cpu").pin_memory(),
+             "dq": torch.empty_like(dq, device="cpu").pin_memory(), "dk": torch.empty_like(dk, device="cpu").pin_memory(),
+             "dv": torch.empty_like(dv, device="cpu").pin_memory()}
+    d_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    E = max(1, args.e2e_steps)
+    with torch.cuda.stream(stream):
+        e2e_ev = []
+        for i in range(E + 3):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            q.copy_(h_in["q"], non_blocking=True)
+            k.copy_(h_in["k"], non_blocking=True)
+            v.copy_(h_in["v"], non_blocking=True)
+            do.copy_(h_in["do"], non_blocking=True)
+            step()
+            for name, t in h_out.items():
+                t.copy_(d_out[name], non_blocking=True)
+            s1.record(stream)
+            if i >= 3:
+                e2e_ev.append((s0, s1))
+        torch.cuda.synchronize(dev)
+        assert fa.fa_check_device_status(stream) == fa.FA_OK
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), world)
+    e2e_value = world * step_flops / (e2e_ms / 1e3) / 1e12
+
+    if rank != 0:
+        return
+    peaks, peak_source = load_peaks()
+    fwd_tf = fwd_flops / (fwd_ms / 1e3) / 1e12
+    bwd_tf = bwd_flops / (bwd_ms / 1e3) / 1e12
+    # dominant kernel: the one with the larger share of the step
+    if bwd_ms >= fwd_ms:
+        dom, dom_tf, dom_name = "bwd", bwd_tf, "fa_bwd_kernel"
+    else:
+        dom, dom_tf, dom_name = "fwd", fwd_tf, "fa_fwd_kernel"
+    peak = peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "achieved": dom_tf, "peak": peak, "unit": "TFLOP/s", "frac": dom_tf / peak,
+                "traffic": recorded_traffic(dom_name, w.name), "kernel": dom_name,
+                "peak_source": f"{peak_source} bf16 sustained (kernel timed inside a long run of steps)",
+                "frac_of_burst_peak": dom_tf / peaks["bf16_tflops"]}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "l2": "flushed before every timed step (256 MiB write, outside the step's events)",
+                   "step": "fa_fwd + fa_bwd (preprocess, main kernel, dQ cast)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "breakdown": {"fwd_kernel_ms": fwd_ms, "fwd_tflops": fwd_tf, "bwd_kernel_ms": bwd_ms, "bwd_tflops": bwd_tf,
+                      "other_ms": step_ms - fwd_ms - bwd_ms,
+                      "fwd_frac_of_sustained_peak": fwd_tf / peak, "bwd_frac_of_sustained_peak": bwd_tf / peak},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * K,
+        "clocks": clock_info,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp_np, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -22,6 +22,18 @@ namespace {
 
 std::atomic<unsigned long long> g_wait_limit_ns{0};
 std::atomic<int> g_debug_stall{0};
+
+// caller-owned events recorded around the main kernels (profiling hook)
+struct TimingEvents {
+  cudaEvent_t fwd_start = nullptr, fwd_stop = nullptr, bwd_start = nullptr, bwd_stop = nullptr;
+};
+std::mutex g_timing_mu;
+TimingEvents g_timing;
+
+TimingEvents timing_events() {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  return g_timing;
+}
 constexpr unsigned long long kDefaultWaitLimitNs = 2000ull * 1000 * 1000;
 
 unsigned long long wait_limit_ns() {
@@ -87,8 +99,12 @@ fa_status launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   auto kernel = fa::fa_fwd_kernel<D, CAUSAL>;
   if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
   const long long grid = (long long)p.num_pairs * BH;
+  const TimingEvents ev = timing_events();
+  if (ev.fwd_start && ev.fwd_stop && cudaEventRecord(ev.fwd_start, stream) != cudaSuccess) return FA_ERR_CUDA;
   kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  if (ev.fwd_start && ev.fwd_stop && cudaEventRecord(ev.fwd_stop, stream) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 template <int D, bool CAUSAL>
@@ -98,8 +114,12 @@ fa_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   auto kernel = fa::fa_bwd_kernel<D, CAUSAL>;
   if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
   const long long grid = (long long)p.nkb * BH;
+  const TimingEvents ev = timing_events();
+  if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_start, stream) != cudaSuccess) return FA_ERR_CUDA;
   kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_stop, stream) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 fa_status launch_preprocess(const void* o, const void* dout, float* delta, float* dq_acc, long long rows, int d,
@@ -135,6 +155,14 @@ const char* fa_status_string(fa_status status) {
 void fa_set_wait_limit_ns(unsigned long long limit_ns) { g_wait_limit_ns.store(limit_ns); }
 
 void fa_debug_stall(int enable) { g_debug_stall.store(enable ? 1 : 0); }
+
+void fa_set_timing_events(cudaEvent_t fwd_start, cudaEvent_t fwd_stop, cudaEvent_t bwd_start, cudaEvent_t bwd_stop) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  g_timing.fwd_start = fwd_start;
+  g_timing.fwd_stop = fwd_stop;
+  g_timing.bwd_start = bwd_start;
+  g_timing.bwd_stop = bwd_stop;
+}
 
 fa_status fa_check_device_status(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;

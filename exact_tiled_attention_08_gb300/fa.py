@@ -67,6 +67,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_set_wait_limit_ns.restype = None
     lib.fa_debug_stall.argtypes = [i]
     lib.fa_debug_stall.restype = None
+    lib.fa_set_timing_events.argtypes = [vp, vp, vp, vp]
+    lib.fa_set_timing_events.restype = None
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     if path is None:
@@ -115,6 +117,22 @@ def fa_set_wait_limit_ns(limit_ns: int) -> None:
 def fa_debug_stall(enable: bool) -> None:
     """Test hook: kernels launched while enabled stall on a barrier nothing signals."""
     load_library().fa_debug_stall(int(bool(enable)))
+
+
+def _event_handle(ev) -> int:
+    if ev is None:
+        return 0
+    if isinstance(ev, torch.cuda.Event):
+        if ev.cuda_event == 0:
+            raise ValueError("record a torch.cuda.Event once before passing it (it is created lazily)")
+        return ev.cuda_event
+    return int(ev)
+
+
+def fa_set_timing_events(fwd_start=None, fwd_stop=None, bwd_start=None, bwd_stop=None) -> None:
+    """Events recorded around the forward kernel and the main backward kernel (profiling)."""
+    load_library().fa_set_timing_events(_event_handle(fwd_start), _event_handle(fwd_stop),
+                                        _event_handle(bwd_start), _event_handle(bwd_stop))
 
 
 def fa_check_device_status(stream=None) -> int:

@@ -145,6 +145,18 @@ void fa_set_wait_limit_ns(unsigned long long limit_ns);
  */
 void fa_debug_stall(int enable);
 
+/*
+ * Profiling hook.  While set, fa_fwd records fwd_start and fwd_stop on its
+ * stream immediately before and after launching its attention kernel, and
+ * fa_bwd records bwd_start and bwd_stop around its main backward kernel (not
+ * around the preprocess or the final dQ cast), so that cudaEventElapsedTime
+ * gives the duration of exactly those kernels.  The events are created and
+ * owned by the caller on the device the calls run on; a null pointer disables
+ * its pair.  Process-wide; call again with nulls to turn it off.
+ */
+void fa_set_timing_events(cudaEvent_t fwd_start, cudaEvent_t fwd_stop, cudaEvent_t bwd_start,
+                          cudaEvent_t bwd_stop);
+
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status status);
 

@@ -26,7 +26,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_workspace_bytes", "fa_check_device_status",
-                     "fa_status_string", "fa_set_wait_limit_ns", "fa_debug_stall"):
+                     "fa_status_string", "fa_set_wait_limit_ns", "fa_debug_stall", "fa_set_timing_events"):
         assert required in names
 
 
