@@ -264,3 +264,97 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward with library-owned scratch, for callers that cannot allocate.
+//
+// fa_bwd needs an fp32 dQ accumulator and the delta vector in device memory
+// that the caller provides.  Some callers cannot provide it when they call
+// the backward: code running inside a runtime that owns all device memory
+// through its own arena and does not let plug-ins call cudaMalloc while it
+// executes, or code that must keep a fixed device-memory footprint once it
+// has started.  fa_bwd_static_scratch takes its scratch from the file-scope
+// array below instead, whose size is fixed when the library is loaded: every
+// device that loads the library holds these FA_STATIC_SCRATCH_BYTES until
+// the process exits, and no call allocates anything.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_fa_static_scratch[FA_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+fa_status static_scratch_on_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_static_scratch_mu);
+  if (!g_static_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_static_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
+    g_static_scratch_ptr[dev] = p;
+  }
+  *out = g_static_scratch_ptr[dev];
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd_static_scratch(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                                float scale, int causal, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  fa_status st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale, causal)) != FA_OK) return st;
+  if (fa_bwd_workspace_bytes(B, H, N, d) > (size_t)FA_STATIC_SCRATCH_BYTES) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  void* scratch = nullptr;
+  if ((st = static_scratch_on_current_device(&scratch)) != FA_OK) return st;
+  const int BH = B * H;
+  const long long rows = (long long)BH * N;
+  // same layout as fa_bwd's workspace: fp32 dQ accumulator, then delta
+  float* dq_acc = static_cast<float*>(scratch);
+  const size_t dq_bytes = ((size_t)rows * d * sizeof(float) + 255) & ~size_t(255);
+  float* delta = reinterpret_cast<float*>(static_cast<char*>(scratch) + dq_bytes);
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_bhnd(&mq, q, BH, N, d) || !encode_bhnd(&mk, k, BH, N, d) || !encode_bhnd(&mv, v, BH, N, d) ||
+      !encode_bhnd(&mdo, dout, BH, N, d))
+    return FA_ERR_CUDA;
+  // the previous call's contents stay in the array: the preprocess rewrites
+  // delta and zeroes the dQ accumulator before anything reads them
+  if ((st = launch_preprocess(o, dout, delta, dq_acc, rows, d, stream)) != FA_OK) return st;
+  fa::BwdParams p;
+  p.lse = lse;
+  p.delta = delta;
+  p.dq_acc = dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.N = N;
+  p.nkb = (N + 127) / 128;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale = scale;
+  p.wait_limit_ns = wait_limit_ns();
+  p.debug_stall = g_debug_stall.load();
+  if (d == 128)
+    st = causal ? launch_bwd<128, true>(mq, mk, mv, mdo, p, BH, stream) : launch_bwd<128, false>(mq, mk, mv, mdo, p, BH, stream);
+  else
+    st = causal ? launch_bwd<64, true>(mq, mk, mv, mdo, p, BH, stream) : launch_bwd<64, false>(mq, mk, mv, mdo, p, BH, stream);
+  if (st != FA_OK) return st;
+  const long long n8 = rows * d / 8;
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  fa::fa_dq_convert_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), scale, n8);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

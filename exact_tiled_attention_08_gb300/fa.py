@@ -61,6 +61,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_bwd_workspace_bytes.restype = sz
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_bwd_static_scratch.restype = i
     lib.fa_check_device_status.argtypes = [vp]
     lib.fa_check_device_status.restype = i
     lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
@@ -182,6 +184,25 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: b
                                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
                                ws_bytes, B, H, N, d, float(scale), int(bool(causal)), _stream_handle(stream))
     _raise(st, "fa_bwd")
+
+
+FA_STATIC_SCRATCH_BYTES = 72 * 1024 * 1024
+
+
+def fa_bwd_static_scratch(q, k, v, o, dout, lse, dq, dk, dv, scale: float, causal: bool, stream=None) -> None:
+    """fa_bwd without a workspace argument, for callers that cannot allocate device
+    memory at call time: the scratch is a fixed array inside the library (see
+    include/fa.h for the size limit, the first-call set-up and the rule that
+    calls overlapping on the GPU race)."""
+    B, H, N, d = _shape4(q, "q")
+    dev = q.device
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, name, torch.bfloat16, (B, H, N, d), dev)
+    _check(lse, "lse", torch.float32, (B, H, N), dev)
+    st = load_library().fa_bwd_static_scratch(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                                              lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                              B, H, N, d, float(scale), int(bool(causal)), _stream_handle(stream))
+    _raise(st, "fa_bwd_static_scratch")
 
 
 # ---------------------------------------------------------------------------

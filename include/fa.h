@@ -119,6 +119,35 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, cudaStream_t stream);
 
 /*
+ * Backward pass with library-owned scratch.  This entry point has no
+ * counterpart on the source pages; it exists for callers that cannot
+ * allocate device memory when they run the backward pass -- for example a
+ * plug-in inside a runtime that hands out device memory only from its own
+ * arena and forbids cudaMalloc during execution, or a program that must keep
+ * a fixed device-memory footprint after start-up.  It computes exactly what
+ * fa_bwd computes, with the same arguments minus the workspace: the fp32 dQ
+ * accumulator and delta live in a fixed array of FA_STATIC_SCRATCH_BYTES
+ * compiled into the library, which every device that loads the library holds
+ * until the process exits.  The call allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine).
+ *
+ * Limit: shapes whose fa_bwd_workspace_bytes(B, H, N, d) exceeds
+ * FA_STATIC_SCRATCH_BYTES (72 MiB; e.g. B*H*N*(d+1)*4 bytes must fit, as for
+ * B=4, H=16, N=2048, d=128) return FA_ERR_INVALID_ARG and run nothing.
+ * Set-up: the first call on a device looks up the array's device address on
+ * that device (cudaGetSymbolAddress, with that device current) and caches it;
+ * make that first call outside any stream capture.  Sharing: every call uses
+ * the same array and the array keeps the last call's contents (each call
+ * re-initialises what it reads).  Calls whose work overlaps on the GPU (on
+ * different streams, or from different threads) race on the array and give
+ * wrong results; calls ordered on one stream do not.
+ */
+#define FA_STATIC_SCRATCH_BYTES (72u * 1024u * 1024u)
+fa_status fa_bwd_static_scratch(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                                float scale, int causal, cudaStream_t stream);
+
+/*
  * Synchronizes `stream`, then returns and clears the current device's status
  * word: FA_OK, or FA_ERR_TIMEOUT if a kernel of this library gave up waiting
  * on one of its barriers since the last check (its outputs are then
