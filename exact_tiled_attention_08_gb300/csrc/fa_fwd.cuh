@@ -15,16 +15,18 @@
 //   warps 4-7  softmax warpgroup of tile 1
 //   warp  8    MMA issuer (one thread) and TMEM owner
 //   warp  9    TMA producer (one thread)
-// Tensor memory (512 columns): S_t at column 128 t (128 fp32 columns; the
-// bf16 probabilities P_t overwrite its first 64 columns), O_t at 256 + d t.
-// Shared memory: Q_0, Q_1 and a ring of NSLOT K/V tiles, all 128 x d bf16
-// with 128-byte swizzle.
+// Tensor memory (512 columns): one score buffer S (128 fp32 columns) that the
+// two tiles use in turn, the bf16 probabilities P_0, P_1 (64 columns each)
+// and the output accumulators O_0, O_1 (d columns each).  Shared memory: Q_0,
+// Q_1 and a ring of K/V tiles, all with 128-byte swizzle.
 //
-// Per key block j the MMA thread issues S_0 = Q_0 K_j^T, S_1 = Q_1 K_j^T, then,
-// as each softmax warpgroup publishes P_t, O_t += P_t V_j.  While warpgroup 0
-// exponentiates S_0 the tensor core works on tile 1 and vice versa.  Because
-// P_t lives in S_t's columns, S_t for block j+1 is issued only after the MMA
-// O_t += P_t V_j has completed.
+// Per key block j the MMA thread issues S_0(j) = Q_0 K_j^T,
+// O_1 += P_1(j-1) V_{j-1}, S_1(j) = Q_1 K_j^T, O_0 += P_0(j) V_j, so each
+// softmax warpgroup exponentiates while the tensor core runs the other
+// tile's two products.  A softmax releases S as soon as it has loaded its
+// scores into registers.  Because every MMA commit covers all earlier MMAs,
+// seeing S_t(j) complete also means O_t += P_t(j-1) V_{j-1} has completed, so
+// the softmax may then overwrite P_t and correct O_t without another wait.
 //
 // Scores are handled in base 2: the softmax works on s * scale * log2(e), so
 // each probability is one ex2; LSE is converted back to natural-log units.
@@ -50,23 +52,24 @@ template <int D>
 struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kTileRows = 128;
-  static constexpr int kTileBytes = kTileRows * D * 2;
-  static constexpr int kAtoms = D / 64;  // 64-column atom columns per tile
-  static constexpr int kSlots = (D == 128) ? 4 : 8;
+  static constexpr int kTileBytes = kTileRows * D * 2;  // Q, K, V tiles
+  static constexpr int kAtoms = D / 64;                 // 64-column atom columns per tile
+  static constexpr int kSlots = (D == 128) ? 5 : 12;
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kSCol0 = 0, kSCol1 = 128;
+  static constexpr uint32_t kSCol = 0, kPCol0 = 128, kPCol1 = 192;
   static constexpr uint32_t kOCol0 = 256, kOCol1 = 256 + D;
-  static constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kSlots * kTileBytes + 256;
+  static constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kSlots * kTileBytes + 512;
 };
 
 struct FwdBarriers {
   uint64_t q_full;
-  uint64_t kv_full[8];
-  uint64_t kv_empty[8];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t pv_done[2];
+  uint64_t kv_full[16];
+  uint64_t kv_empty[16];
+  uint64_t s_full[2];   // S holds tile t's scores (MMA commit)
+  uint64_t s_free;      // the tile that used S last has loaded it (128 softmax threads)
+  uint64_t p_full[2];   // P_t written, O_t corrected (128 softmax threads)
+  uint64_t pv_done[2];  // O_t += P_t V complete (MMA commit)
   uint64_t drain;
   uint64_t never;  // signalled by nothing: the debug stall waits on it
   uint32_t tmem_base;
@@ -84,7 +87,8 @@ struct FwdParams {
 };
 
 // wait sites reported in the status word
-enum : int { kSiteStall = 0, kSiteFwdProducer = 1, kSiteFwdQ, kSiteFwdK, kSiteFwdV, kSiteFwdPvDone, kSiteFwdP, kSiteFwdS, kSiteFwdO };
+enum : int { kSiteStall = 0, kSiteFwdProducer = 1, kSiteFwdQ, kSiteFwdK, kSiteFwdV, kSiteFwdSFree, kSiteFwdP,
+             kSiteFwdS, kSiteFwdO };
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
@@ -122,6 +126,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&bar->p_full[t], 128);
       mbar_init(&bar->pv_done[t], 1);
     }
+    mbar_init(&bar->s_free, 128);
     mbar_init(&bar->drain, 1);
     mbar_init(&bar->never, 1);
     bar->abort_flag = 0;
@@ -144,6 +149,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 9) {
     // ------------------------------------------------------------------ TMA producer
+    // fill order = consumption order: K_0, V_0, K_1, V_1, ...
     if (lane == 0) {
       int fill = 0;
       mbar_arrive_expect_tx(&bar->q_full, C::kTileBytes * (has1 ? 2 : 1));
@@ -184,63 +190,81 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t qdesc1 = sdesc_sw128(sq + C::kTileBytes, 16, 1024);
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
-      int cons = 0;
+      int cons = 0;     // ring slots acquired (in fill order)
+      int s_uses = 0;   // S buffer fills issued so far
       bool ok = !(p.debug_stall && !wait_bounded(&bar->never, 0, ctx, kSiteStall));
       ok = ok && wait_bounded(&bar->q_full, 0, ctx, kSiteFwdQ);
+      auto acquire = [&](int site) -> int {
+        const int s = cons % C::kSlots;
+        if (!wait_bounded(&bar->kv_full[s], (cons / C::kSlots) & 1, ctx, site)) {
+          ok = false;
+          return 0;
+        }
+        tc_fence_after();
+        ++cons;
+        return s;
+      };
+      // S = Q_t K^T into the shared score buffer, once its previous user has loaded it
+      auto issue_s = [&](int t, uint32_t kslot) {
+        if (s_uses > 0) {
+          if (!wait_bounded(&bar->s_free, (s_uses - 1) & 1, ctx, kSiteFwdSFree)) {
+            ok = false;
+            return;
+          }
+          tc_fence_after();
+        }
+        const uint64_t kdesc = sdesc_sw128(skv + kslot * C::kTileBytes, 16, 1024);
+        const uint64_t qd = t ? qdesc1 : qdesc0;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + C::kSCol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar->s_full[t]);
+        ++s_uses;
+      };
+      // O_t += P_t V_j, once the softmax of tile t has written P_t(j)
+      auto issue_pv = [&](int t, int j, uint32_t vslot) {
+        if (!wait_bounded(&bar->p_full[t], j & 1, ctx, kSiteFwdP)) {
+          ok = false;
+          return;
+        }
+        tc_fence_after();
+        const uint64_t vdesc = sdesc_sw128(skv + vslot * C::kTileBytes, 16384, 1024);
+        const uint32_t dcol = tmem + (t ? C::kOCol1 : C::kOCol0);
+        const uint32_t pcol = tmem + (t ? C::kPCol1 : C::kPCol0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 2048) >> 4), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar->pv_done[t]);
+      };
+      uint32_t vprev = 0;  // slot of V_{j-1}, still needed by tile 1
       for (int j = 0; ok && j < nb_max; ++j) {
-        // ---- S_t = Q_t K_j^T
-        int s = cons % C::kSlots;
-        if (!wait_bounded(&bar->kv_full[s], (cons / C::kSlots) & 1, ctx, kSiteFwdK)) break;
-        tc_fence_after();
-        const uint64_t kdesc = sdesc_sw128(skv + s * C::kTileBytes, 16, 1024);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (j < (t ? nb1 : nb0)) {
-            if (j > 0) {
-              if (!wait_bounded(&bar->pv_done[t], (j - 1) & 1, ctx, kSiteFwdPvDone)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-            }
-            const uint64_t qd = t ? qdesc1 : qdesc0;
-            const uint32_t dcol = tmem + (t ? C::kSCol1 : C::kSCol0);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-              mma_bf16_ss(dcol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&bar->s_full[t]);
-          }
-        }
+        const uint32_t ks = acquire(kSiteFwdK);
         if (!ok) break;
-        mma_commit(&bar->kv_empty[s]);
-        ++cons;
-        // ---- O_t += P_t V_j
-        s = cons % C::kSlots;
-        if (!wait_bounded(&bar->kv_full[s], (cons / C::kSlots) & 1, ctx, kSiteFwdV)) break;
-        tc_fence_after();
-        const uint64_t vdesc = sdesc_sw128(skv + s * C::kTileBytes, 16384, 1024);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (j < (t ? nb1 : nb0)) {
-            if (!wait_bounded(&bar->p_full[t], j & 1, ctx, kSiteFwdP)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t dcol = tmem + (t ? C::kOCol1 : C::kOCol0);
-            const uint32_t pcol = tmem + (t ? C::kSCol1 : C::kSCol0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_bf16_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 2048) >> 4), id_pv,
-                          (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&bar->pv_done[t]);
-          }
-        }
+        if (j < nb0) issue_s(0, ks);
         if (!ok) break;
-        mma_commit(&bar->kv_empty[s]);
-        ++cons;
+        if (j > 0 && j - 1 < nb1) {
+          issue_pv(1, j - 1, vprev);
+          if (!ok) break;
+          mma_commit(&bar->kv_empty[vprev]);
+        }
+        if (j < nb1) issue_s(1, ks);
+        if (!ok) break;
+        mma_commit(&bar->kv_empty[ks]);
+        const uint32_t vs = acquire(kSiteFwdV);
+        if (!ok) break;
+        if (j < nb0) issue_pv(0, j, vs);
+        if (!ok) break;
+        if (j < nb1) {
+          vprev = vs;  // released after tile 1's product in the next step
+        } else {
+          mma_commit(&bar->kv_empty[vs]);
+        }
+      }
+      if (ok && nb1 == nb_max && nb1 > 0) {
+        issue_pv(1, nb1 - 1, vprev);
+        if (ok) mma_commit(&bar->kv_empty[vprev]);
       }
       // everything issued must complete before the tensor memory is released
       mma_commit(&bar->drain);
@@ -255,7 +279,8 @@ __global__ void __launch_bounds__(320, 1)
     const int nb = t ? nb1 : nb0;
     const int row_g = q0 + 128 * t + r;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + (t ? C::kSCol1 : C::kSCol0) + lane_off;
+    const uint32_t tS = tmem + C::kSCol + lane_off;
+    const uint32_t tP = tmem + (t ? C::kPCol1 : C::kPCol0) + lane_off;
     const uint32_t tO = tmem + (t ? C::kOCol1 : C::kOCol0) + lane_off;
     const float sl2 = p.scale_log2;
     float m = -CUDART_INF_F;  // exponent reference (log2 units), a stale running max
@@ -273,6 +298,9 @@ __global__ void __launch_bounds__(320, 1)
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
+      // the scores are in registers: the other tile's scores may now overwrite S
+      tc_fence_before();
+      mbar_arrive(&bar->s_free);
 
       const int kbase = j * 128;
       const bool tail = kbase + 128 > N;
@@ -283,9 +311,25 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < 128; ++c)
           if (c > last) sr[c >> 5][c & 31] = __float_as_uint(-CUDART_INF_F);
       }
-      float mx = __uint_as_float(sr[0][0]);
+      // row maximum as a tree of 3-input maxima
+      float mx;
+      {
+        float t1[43];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
+        for (int i = 0; i < 42; ++i)
+          t1[i] = max3(__uint_as_float(sr[(3 * i) >> 5][(3 * i) & 31]),
+                       __uint_as_float(sr[(3 * i + 1) >> 5][(3 * i + 1) & 31]),
+                       __uint_as_float(sr[(3 * i + 2) >> 5][(3 * i + 2) & 31]));
+        t1[42] = fmaxf(__uint_as_float(sr[3][30]), __uint_as_float(sr[3][31]));
+        float t2[15];
+#pragma unroll
+        for (int i = 0; i < 14; ++i) t2[i] = max3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
+        t2[14] = t1[42];
+        float t3[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) t3[i] = max3(t2[3 * i], t2[3 * i + 1], t2[3 * i + 2]);
+        mx = max3(max3(t3[0], t3[1], t3[2]), t3[3], t3[4]);
+      }
       const float m_new = fmaxf(m, mx * sl2);
       // conditional rescale: move the exponent reference only when the row
       // maximum rose by more than the threshold (always on the first block)
@@ -301,34 +345,38 @@ __global__ void __launch_bounds__(320, 1)
           m = m_new;
         }
       }
-      // p = 2^(s c - m) two at a time (packed fp32x2 FMA/adds).  Two row sums
-      // are kept: `l` of the fp32 probabilities (for the LSE) and `l_mma` of
-      // the bf16-rounded probabilities that the P V product actually uses (for
-      // the normalisation of O, so a dominant probability's rounding cancels).
+      // p = 2^(s c - m) two at a time.  Two row sums are kept: `l` of the fp32
+      // probabilities (for the LSE) and `l_mma` of the bf16-rounded ones that
+      // the P V product uses (for the normalisation of O, so that the rounding
+      // of a dominant probability cancels); four partial sums each.
       const float2 c2 = make_float2(sl2, sl2);
       const float2 mneg2 = make_float2(-m, -m);
-      float2 acc = make_float2(0.f, 0.f), acc_mma = make_float2(0.f, 0.f);
+      float2 acc[4], acc_mma[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) acc[a] = acc_mma[a] = make_float2(0.f, 0.f);
+      uint32_t pk[4][16];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
                                       c2, mneg2);
           const float p0 = ex2_approx(x.x);
           const float p1 = ex2_approx(x.y);
-          pk[i] = pack_bf16x2(p0, p1);
-          acc = __fadd2_rn(acc, make_float2(p0, p1));
-          acc_mma = __fadd2_rn(acc_mma, make_float2(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xffff0000u)));
+          pk[c][i] = pack_bf16x2(p0, p1);
+          acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
+          acc_mma[i & 3] = __fadd2_rn(acc_mma[i & 3], make_float2(__uint_as_float(pk[c][i] << 16),
+                                                                 __uint_as_float(pk[c][i] & 0xffff0000u)));
         }
-        tmem_st16(tS + 16 * c, pk);
       }
-      l = l * alpha + (acc.x + acc.y);
-      l_mma = l_mma * alpha + (acc_mma.x + acc_mma.y);
+      const float2 accs = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+      const float2 accm = __fadd2_rn(__fadd2_rn(acc_mma[0], acc_mma[1]), __fadd2_rn(acc_mma[2], acc_mma[3]));
+      l = l * alpha + (accs.x + accs.y);
+      l_mma = l_mma * alpha + (accm.x + accm.y);
+      // O_t += P_t(j-1) V_{j-1} completed before S_t(j) did (each commit covers
+      // every earlier MMA), so P_t may be overwritten and O_t corrected now.
       if (rescale_warp) {
-        // O_t accumulated through block j-1 is complete (the commit behind
-        // s_full covers it) and the next P V waits for p_full, so the
-        // correction O <- alpha O can be applied in place here.
+        // correction O <- alpha O, in place in tensor memory
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
@@ -339,12 +387,15 @@ __global__ void __launch_bounds__(320, 1)
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
           tmem_st32(tO + 32 * c, ov);
         }
+        tmem_wait_st();
       }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_st16(tP + 16 * c, pk[c]);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar->p_full[t]);
     }
-    // epilogue: O = o / l, LSE = (m + log2 l) ln 2
+    // epilogue: O = o / l_mma, LSE = (m + log2 l) ln 2
     if (alive) {
       if (__all_sync(0xffffffffu, wait_bounded(&bar->pv_done[t], (nb - 1) & 1, ctx, kSiteFwdO))) {
         tc_fence_after();
