@@ -10,23 +10,25 @@
 // conditional rescaling.
 //
 // One CTA owns two query tiles of 128 rows (a "tile pair") of one (batch,
-// head).  Warp roles (320 threads):
+// head).  Warp roles (352 threads):
 //   warps 0-3  softmax warpgroup of tile 0 (thread = query row)
 //   warps 4-7  softmax warpgroup of tile 1
-//   warp  8    MMA issuer (one thread) and TMEM owner
+//   warp  8    issues the score products S = Q K^T (one thread); TMEM owner
 //   warp  9    TMA producer (one thread)
+//   warp  10   issues the output products O += P V (one thread)
+// The MMA queue of an SM is shallow: a thread that waits or keeps books
+// between groups of MMAs leaves the tensor core idle, so the two kinds of
+// product are issued by two threads whose waits overlap each other's MMAs.
 // Tensor memory (512 columns): one score buffer S (128 fp32 columns) that the
 // two tiles use in turn, the bf16 probabilities P_0, P_1 (64 columns each)
 // and the output accumulators O_0, O_1 (d columns each).  Shared memory: Q_0,
 // Q_1 and a ring of K/V tiles, all with 128-byte swizzle.
 //
-// Per key block j the MMA thread issues S_0(j) = Q_0 K_j^T,
-// O_1 += P_1(j-1) V_{j-1}, S_1(j) = Q_1 K_j^T, O_0 += P_0(j) V_j, so each
-// softmax warpgroup exponentiates while the tensor core runs the other
-// tile's two products.  A softmax releases S as soon as it has loaded its
-// scores into registers.  Because every MMA commit covers all earlier MMAs,
-// seeing S_t(j) complete also means O_t += P_t(j-1) V_{j-1} has completed, so
-// the softmax may then overwrite P_t and correct O_t without another wait.
+// Per key block j the tiles alternate on S: S_0(j), S_1(j), S_0(j+1), ...; a
+// softmax releases S as soon as it has loaded its scores into registers, so
+// each warpgroup exponentiates while the tensor core computes the other
+// tile's scores and output products.  Before overwriting P_t and correcting
+// O_t a softmax waits until O_t += P_t(j-1) V_{j-1} has completed.
 //
 // Scores are handled in base 2: the softmax works on s * scale * log2(e), so
 // each probability is one ex2; LSE is converted back to natural-log units.
@@ -55,7 +57,7 @@ struct FwdCfg {
   static constexpr int kTileBytes = kTileRows * D * 2;  // Q, K, V tiles
   static constexpr int kAtoms = D / 64;                 // 64-column atom columns per tile
   static constexpr int kSlots = (D == 128) ? 5 : 12;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSCol = 0, kPCol0 = 128, kPCol1 = 192;
   static constexpr uint32_t kOCol0 = 256, kOCol1 = 256 + D;
@@ -70,7 +72,7 @@ struct FwdBarriers {
   uint64_t s_free;      // the tile that used S last has loaded it (128 softmax threads)
   uint64_t p_full[2];   // P_t written, O_t corrected (128 softmax threads)
   uint64_t pv_done[2];  // O_t += P_t V complete (MMA commit)
-  uint64_t drain;
+  uint64_t drain[2];    // one per issuing thread
   uint64_t never;  // signalled by nothing: the debug stall waits on it
   uint32_t tmem_base;
   int abort_flag;
@@ -88,10 +90,10 @@ struct FwdParams {
 
 // wait sites reported in the status word
 enum : int { kSiteStall = 0, kSiteFwdProducer = 1, kSiteFwdQ, kSiteFwdK, kSiteFwdV, kSiteFwdSFree, kSiteFwdP,
-             kSiteFwdS, kSiteFwdO };
+             kSiteFwdS, kSiteFwdO, kSiteFwdPvDone };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
   using C = FwdCfg<D>;
@@ -127,7 +129,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&bar->pv_done[t], 1);
     }
     mbar_init(&bar->s_free, 128);
-    mbar_init(&bar->drain, 1);
+    mbar_init(&bar->drain[0], 1);
+    mbar_init(&bar->drain[1], 1);
     mbar_init(&bar->never, 1);
     bar->abort_flag = 0;
     fence_mbar_init();
@@ -183,92 +186,81 @@ __global__ void __launch_bounds__(320, 1)
     }
     __syncwarp();
   } else if (warp == 8) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ S issuer
+    // K_j is ring fill 2j; S(k) waits until the tile that used S before has loaded it
     if (lane == 0) {
       const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
       const uint64_t qdesc0 = sdesc_sw128(sq, 16, 1024);
       const uint64_t qdesc1 = sdesc_sw128(sq + C::kTileBytes, 16, 1024);
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
-      int cons = 0;     // ring slots acquired (in fill order)
-      int s_uses = 0;   // S buffer fills issued so far
+      int s_uses = 0;
       bool ok = !(p.debug_stall && !wait_bounded(&bar->never, 0, ctx, kSiteStall));
       ok = ok && wait_bounded(&bar->q_full, 0, ctx, kSiteFwdQ);
-      auto acquire = [&](int site) -> int {
-        const int s = cons % C::kSlots;
-        if (!wait_bounded(&bar->kv_full[s], (cons / C::kSlots) & 1, ctx, site)) {
-          ok = false;
-          return 0;
-        }
-        tc_fence_after();
-        ++cons;
-        return s;
-      };
-      // S = Q_t K^T into the shared score buffer, once its previous user has loaded it
-      auto issue_s = [&](int t, uint32_t kslot) {
-        if (s_uses > 0) {
-          if (!wait_bounded(&bar->s_free, (s_uses - 1) & 1, ctx, kSiteFwdSFree)) {
-            ok = false;
-            return;
-          }
-          tc_fence_after();
-        }
-        const uint64_t kdesc = sdesc_sw128(skv + kslot * C::kTileBytes, 16, 1024);
-        const uint64_t qd = t ? qdesc1 : qdesc0;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + C::kSCol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bar->s_full[t]);
-        ++s_uses;
-      };
-      // O_t += P_t V_j, once the softmax of tile t has written P_t(j)
-      auto issue_pv = [&](int t, int j, uint32_t vslot) {
-        if (!wait_bounded(&bar->p_full[t], j & 1, ctx, kSiteFwdP)) {
-          ok = false;
-          return;
-        }
-        tc_fence_after();
-        const uint64_t vdesc = sdesc_sw128(skv + vslot * C::kTileBytes, 16384, 1024);
-        const uint32_t dcol = tmem + (t ? C::kOCol1 : C::kOCol0);
-        const uint32_t pcol = tmem + (t ? C::kPCol1 : C::kPCol0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 2048) >> 4), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar->pv_done[t]);
-      };
-      uint32_t vprev = 0;  // slot of V_{j-1}, still needed by tile 1
       for (int j = 0; ok && j < nb_max; ++j) {
-        const uint32_t ks = acquire(kSiteFwdK);
-        if (!ok) break;
-        if (j < nb0) issue_s(0, ks);
-        if (!ok) break;
-        if (j > 0 && j - 1 < nb1) {
-          issue_pv(1, j - 1, vprev);
-          if (!ok) break;
-          mma_commit(&bar->kv_empty[vprev]);
+        const int f = 2 * j;
+        const int ks = f % C::kSlots;
+        if (!wait_bounded(&bar->kv_full[ks], (f / C::kSlots) & 1, ctx, kSiteFwdK)) break;
+        const uint64_t kdesc = sdesc_sw128(skv + ks * C::kTileBytes, 16, 1024);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j < (t ? nb1 : nb0)) {
+            if (s_uses > 0 && !wait_bounded(&bar->s_free, (s_uses - 1) & 1, ctx, kSiteFwdSFree)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t qd = t ? qdesc1 : qdesc0;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+              mma_bf16_ss(tmem + C::kSCol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bar->s_full[t]);
+            ++s_uses;
+          }
         }
-        if (j < nb1) issue_s(1, ks);
         if (!ok) break;
         mma_commit(&bar->kv_empty[ks]);
-        const uint32_t vs = acquire(kSiteFwdV);
-        if (!ok) break;
-        if (j < nb0) issue_pv(0, j, vs);
-        if (!ok) break;
-        if (j < nb1) {
-          vprev = vs;  // released after tile 1's product in the next step
-        } else {
-          mma_commit(&bar->kv_empty[vs]);
-        }
-      }
-      if (ok && nb1 == nb_max && nb1 > 0) {
-        issue_pv(1, nb1 - 1, vprev);
-        if (ok) mma_commit(&bar->kv_empty[vprev]);
       }
       // everything issued must complete before the tensor memory is released
-      mma_commit(&bar->drain);
-      wait_drain(&bar->drain, 0, kDrainLimitNs);
+      mma_commit(&bar->drain[0]);
+      wait_drain(&bar->drain[0], 0, kDrainLimitNs);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------------ P V issuer
+    // V_j is ring fill 2j+1; O_t += P_t(j) V_j once the softmax of tile t wrote P_t(j)
+    if (lane == 0) {
+      const uint32_t skv = smem_u32(sKV);
+      constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
+      bool ok = true;
+      for (int j = 0; ok && j < nb_max; ++j) {
+        const int f = 2 * j + 1;
+        const int vs = f % C::kSlots;
+        if (!wait_bounded(&bar->kv_full[vs], (f / C::kSlots) & 1, ctx, kSiteFwdV)) break;
+        const uint64_t vdesc = sdesc_sw128(skv + vs * C::kTileBytes, 16384, 1024);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j < (t ? nb1 : nb0)) {
+            if (!wait_bounded(&bar->p_full[t], j & 1, ctx, kSiteFwdP)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t dcol = tmem + (t ? C::kOCol1 : C::kOCol0);
+            const uint32_t pcol = tmem + (t ? C::kPCol1 : C::kPCol0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 2048) >> 4), id_pv,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bar->pv_done[t]);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bar->kv_empty[vs]);
+      }
+      mma_commit(&bar->drain[1]);
+      wait_drain(&bar->drain[1], 0, kDrainLimitNs);
     }
     __syncwarp();
   } else {
@@ -373,8 +365,14 @@ __global__ void __launch_bounds__(320, 1)
       const float2 accm = __fadd2_rn(__fadd2_rn(acc_mma[0], acc_mma[1]), __fadd2_rn(acc_mma[2], acc_mma[3]));
       l = l * alpha + (accs.x + accs.y);
       l_mma = l_mma * alpha + (accm.x + accm.y);
-      // O_t += P_t(j-1) V_{j-1} completed before S_t(j) did (each commit covers
-      // every earlier MMA), so P_t may be overwritten and O_t corrected now.
+      // P_t and O_t are in use until O_t += P_t(j-1) V_{j-1} has completed
+      if (j > 0) {
+        if (!__all_sync(0xffffffffu, wait_bounded(&bar->pv_done[t], (j - 1) & 1, ctx, kSiteFwdPvDone))) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+      }
       if (rescale_warp) {
         // correction O <- alpha O, in place in tensor memory
 #pragma unroll 1
