@@ -59,72 +59,130 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------------------
+// preprocess of fa_bwd: per row of each (batch, head), padded to a whole
+// number of 128-row blocks (Npad = 128 ceil(N / 128)):
+//   delta_pad[bh][n] = sum_c dO_nc O_nc      (0 for n >= N)
+//   lse2_pad[bh][n]  = LSE_n * log2(e)       (+inf for n >= N, so P = 0 there)
+// and the fp32 dQ accumulator rows are zeroed.  The padded, 128-aligned rows
+// let the main kernel bring both vectors in with TMA next to each Q tile.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256)
+    fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                       const float* __restrict__ lse, float* __restrict__ delta_pad, float* __restrict__ lse2_pad,
+                       float* __restrict__ dq_acc, int N, int Npad, long long padded_rows) {
+  constexpr int kThreadsPerRow = D / 8;
+  constexpr int kRowsPerPass = 256 / kThreadsPerRow;
+  const int sub = threadIdx.x % kThreadsPerRow;
+  const int rloc = threadIdx.x / kThreadsPerRow;
+  for (long long base = (long long)blockIdx.x * kRowsPerPass; base < padded_rows;
+       base += (long long)gridDim.x * kRowsPerPass) {
+    const long long prow = base + rloc;  // padded row index bh * Npad + n
+    const long long bh = prow / Npad;
+    const int n = (int)(prow - bh * Npad);
+    const bool in_range = prow < padded_rows;
+    const bool valid = in_range && n < N;
+    const long long row = bh * N + n;  // unpadded row
+    float s = 0.f;
+    if (valid) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D) + sub);
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + row * D) + sub);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 fa2 = __bfloat1622float2(a2[i]);
+        const float2 fb2 = __bfloat1622float2(b2[i]);
+        s = fmaf(fa2.x, fb2.x, s);
+        s = fmaf(fa2.y, fb2.y, s);
+      }
+    }
+#pragma unroll
+    for (int off = kThreadsPerRow / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (in_range && sub == 0) {
+      delta_pad[prow] = valid ? s : 0.f;
+      lse2_pad[prow] = valid ? __ldg(lse + row) * 1.4426950408889634f : CUDART_INF_F;
+    }
+    if (valid) {
+      float4* z = reinterpret_cast<float4*>(dq_acc + row * D) + 2 * sub;
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // main backward kernel: one CTA per (key block j, batch, head).
 //
 // K_j and V_j (128 keys) stay in shared memory; the query blocks i (all of
-// them, or i >= j when causal) stream Q_i and dO_i through a ring.  Per query
-// block, in the transposed orientation (TMEM lane = key, column = query):
-//   S^T  = K_j Q_i^T                       (tcgen05, smem x smem -> TMEM)
-//   dP^T = V_j dO_i^T                      (tcgen05, smem x smem -> TMEM)
-//   P^T  = 2^(S^T scale log2e - LSE_i log2e), masked on the causal diagonal
-//   dS^T = P^T o (dP^T - delta_i)          (elementwise warps, thread = key)
-//   dV  += P^T dO_i                        (P^T as bf16 in TMEM over S^T)
-//   dK  += dS^T Q_i                        (dS^T as bf16 in shared memory)
-//   dQ_i = dS K_j                          (the same dS^T tile read M-major)
-// and dQ_i is added into the fp32 accumulator in global memory.  dK, dV
-// accumulate in TMEM across all query blocks and are written once.
+// them, or i >= j when causal) stream Q_i (with its rows' LSE log2(e) and
+// delta) and dO_i through a ring.  Per query block, in the transposed
+// orientation (TMEM lane = key, column = query):
+//   S^T  = K_j Q_i^T, dP^T = V_j dO_i^T          (issuer A)
+//   P^T  = 2^(S^T scale log2e - LSE_i log2e), masked on the causal diagonal,
+//   dS^T = P^T o (dP^T - delta_i)                  (elementwise warps, thread = key)
+//   dV  += P^T dO_i, dK += dS^T Q_i, dQ_i = dS K_j  (issuer B)
+// and the dQ warpgroup adds dQ_i into the fp32 accumulator in global memory
+// with TMA bulk reduce-adds.  dK, dV accumulate in TMEM across all query
+// blocks and are written once at the end.
 //
-// Warp roles (320 threads): warps 0-7 form two warpgroups g = 0, 1 that own
-// query columns [64 g, 64 g + 64) of the elementwise step and columns
-// [g d/2, (g+1) d/2) of the dQ read-out; warp 8 issues MMAs and owns TMEM;
-// warp 9 issues TMA copies.
-// Tensor memory: dK at column 0, dV at d, S^T at 2d, dP^T at 2d + 128; dQ_i
-// reuses the dP^T columns once the elementwise step has consumed them.
+// Warp roles (480 threads):
+//   warps 0-7   elementwise: warpgroup g owns query columns [64 g, 64 g + 64)
+//   warp  8     issuer A (S^T, dP^T) and TMEM owner
+//   warp  9     TMA producer
+//   warp  10    issuer B (dV, dK, dQ)
+//   warps 11-14 dQ warpgroup: TMEM -> shared staging -> TMA reduce-add
+// Tensor memory: dK at column 0, dV at d, S^T at 2d, dP^T at 2d + 128.  The
+// bf16 P^T of query group G (queries 16G..16G+15) is written over the first 8
+// of that group's own S^T columns, which only the writing thread has read;
+// dQ_i goes into the dP^T columns once the elementwise step has read them.
 // ---------------------------------------------------------------------------
 template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kAtoms = D / 64;
-  static constexpr int kSlots = (D == 128) ? 3 : 6;  // Q / dO ring
-  static constexpr int kDsBytes = 128 * 128 * 2;     // dS^T tile: 2 atom columns of 64 queries
-  static constexpr int kThreads = 320;
+  static constexpr int kSlots = (D == 128) ? 3 : 6;   // Q / dO ring
+  static constexpr int kStatBytes = 1024;             // LSE*log2e and delta of one query block
+  static constexpr int kDsBytes = 128 * 128 * 2;      // dS^T tile: 2 atom columns of 64 queries
+  static constexpr int kStageBytes = 4 * 4096;        // dQ staging: 32 rows x 32 fp32 per dQ warp
+  static constexpr int kThreads = 480;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kDkCol = 0, kDvCol = D, kSCol = 2 * D, kDpCol = 2 * D + 128;
-  static constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kSlots * kTileBytes + kDsBytes + 2 * 2 * 128 * 4 + 256;
+  static constexpr int kSmemBytes =
+      1024 + 2 * kTileBytes + kSlots * kTileBytes + kDsBytes + kStageBytes + kSlots * kStatBytes + 512;
 };
 
 struct BwdBarriers {
   uint64_t kv_full;
   uint64_t ring_full[8];
   uint64_t ring_empty[8];
-  uint64_t s_full, dp_full, s_read, ew_done, dv_done, dq_full, dq_free, acc_done, drain;
+  uint64_t s_full, dp_full, ew_done, dv_done, dq_full, dq_free, acc_done;
+  uint64_t drain[2];
   uint64_t never;  // signalled by nothing: the debug stall waits on it
   uint32_t tmem_base;
   int abort_flag;
 };
 
 struct BwdParams {
-  const float* lse;
-  const float* delta;
-  float* dq_acc;
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
+  __nv_bfloat16* dk_out;
+  __nv_bfloat16* dv_out;
   int N;
   int nkb;           // key (and query) blocks per head
   float scale_log2;  // scale * log2(e)
   float scale;
   uint64_t wait_limit_ns;
-  int debug_stall;  // nonzero: the MMA thread first waits on `never` (tests the timeout path)
+  int debug_stall;  // nonzero: issuer A first waits on `never` (tests the timeout path)
 };
 
 enum : int { kSiteBwdProducer = 16, kSiteBwdKV, kSiteBwdQ, kSiteBwdDo, kSiteBwdDvDone, kSiteBwdDqFree, kSiteBwdEw,
-             kSiteBwdS, kSiteBwdDp, kSiteBwdDq, kSiteBwdAcc, kSiteBwdSRead };
+             kSiteBwdS, kSiteBwdDp, kSiteBwdDq, kSiteBwdAcc, kSiteBwdDsFree };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(480, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap map_lse2, const __grid_constant__ CUtensorMap map_delta,
+                  const __grid_constant__ CUtensorMap map_dqacc, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -132,8 +190,9 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sV = smem + C::kTileBytes;
   uint8_t* sRing = smem + 2 * C::kTileBytes;
   uint8_t* sDS = sRing + C::kSlots * C::kTileBytes;
-  float* sRowStat = reinterpret_cast<float*>(sDS + C::kDsBytes);  // [2 buffers][lse2 128 | delta 128]
-  BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(sRowStat + 2 * 2 * 128);
+  uint8_t* sStage = sDS + C::kDsBytes;
+  uint8_t* sStat = sStage + C::kStageBytes;  // per ring slot: LSE*log2e [128] then delta [128]
+  BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(sStat + C::kSlots * C::kStatBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N;
@@ -151,13 +210,13 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(&bar->s_full, 1);
     mbar_init(&bar->dp_full, 1);
-    mbar_init(&bar->s_read, 256);
     mbar_init(&bar->ew_done, 256);
     mbar_init(&bar->dv_done, 1);
     mbar_init(&bar->dq_full, 1);
-    mbar_init(&bar->dq_free, 256);
+    mbar_init(&bar->dq_free, 128);
     mbar_init(&bar->acc_done, 1);
-    mbar_init(&bar->drain, 1);
+    mbar_init(&bar->drain[0], 1);
+    mbar_init(&bar->drain[1], 1);
     mbar_init(&bar->never, 1);
     bar->abort_flag = 0;
     fence_mbar_init();
@@ -171,6 +230,8 @@ __global__ void __launch_bounds__(320, 1)
     tma_prefetch_map(&map_k);
     tma_prefetch_map(&map_v);
     tma_prefetch_map(&map_do);
+    tma_prefetch_map(&map_lse2);
+    tma_prefetch_map(&map_delta);
   }
   tc_fence_before();
   __syncthreads();
@@ -180,6 +241,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 9) {
     // ------------------------------------------------------------------ TMA producer
+    // ring fills: Q_i (with its LSE*log2e and delta rows) at 2 it, dO_i at 2 it + 1
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar->kv_full, 2 * C::kTileBytes);
       for (int a = 0; a < C::kAtoms; ++a) {
@@ -197,10 +259,14 @@ __global__ void __launch_bounds__(320, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bar->ring_full[s], C::kTileBytes);
+          mbar_arrive_expect_tx(&bar->ring_full[s], C::kTileBytes + (which ? 0 : C::kStatBytes));
           const CUtensorMap* map = which ? &map_do : &map_q;
           for (int a = 0; a < C::kAtoms; ++a)
             tma_load_3d(sRing + s * C::kTileBytes + a * 16384, map, &bar->ring_full[s], a * 64, i * 128, bh);
+          if (!which) {
+            tma_load_2d(sStat + s * C::kStatBytes, &map_lse2, &bar->ring_full[s], i * 128, bh);
+            tma_load_2d(sStat + s * C::kStatBytes + 512, &map_delta, &bar->ring_full[s], i * 128, bh);
+          }
           ++fill;
         }
       }
@@ -214,26 +280,19 @@ __global__ void __launch_bounds__(320, 1)
     }
     __syncwarp();
   } else if (warp == 8) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ issuer A: S^T, dP^T
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t id_v = idesc_bf16_f32(128, D, false, true);     // dV (A = P^T in TMEM), dK
-      constexpr uint32_t id_q = idesc_bf16_f32(128, D, true, true);      // dQ (A = dS, M-major)
+      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       const uint32_t ring = smem_u32(sRing);
       const uint64_t kdesc = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16, 1024);
-      const uint64_t kdesc_mn = sdesc_sw128(smem_u32(sK), 16384, 1024);
-      const uint64_t dsdesc_k = sdesc_sw128(smem_u32(sDS), 16, 1024);
-      const uint64_t dsdesc_mn = sdesc_sw128(smem_u32(sDS), 16384, 1024);
       const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDpCol;
-      const uint32_t tDK = tmem + C::kDkCol, tDV = tmem + C::kDvCol;
-      int cons = 0;
       bool ok = !(p.debug_stall && !wait_bounded(&bar->never, 0, ctx, kSiteStall));
       ok = ok && wait_bounded(&bar->kv_full, 0, ctx, kSiteBwdKV);
       for (int it = 0; ok && it < n_it; ++it) {
-        // ---- S^T = K Q_i^T
-        const int sq = cons % C::kSlots;
-        if (!wait_bounded(&bar->ring_full[sq], (cons / C::kSlots) & 1, ctx, kSiteBwdQ)) break;
+        // S^T = K Q_i^T, once dV has consumed the previous P^T held in these columns
+        const int fq = 2 * it, sq = fq % C::kSlots;
+        if (!wait_bounded(&bar->ring_full[sq], (fq / C::kSlots) & 1, ctx, kSiteBwdQ)) break;
         if (it > 0 && !wait_bounded(&bar->dv_done, (it - 1) & 1, ctx, kSiteBwdDvDone)) break;
         tc_fence_after();
         const uint64_t qdesc = sdesc_sw128(ring + sq * C::kTileBytes, 16, 1024);
@@ -243,9 +302,9 @@ __global__ void __launch_bounds__(320, 1)
           mma_bf16_ss(tS, kdesc + off, qdesc + off, id_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar->s_full);
-        // ---- dP^T = V dO_i^T (into the columns dQ_{i-1} occupied)
-        const int sd = (cons + 1) % C::kSlots;
-        if (!wait_bounded(&bar->ring_full[sd], ((cons + 1) / C::kSlots) & 1, ctx, kSiteBwdDo)) break;
+        // dP^T = V dO_i^T, once the previous dQ has been read out of these columns
+        const int fd = 2 * it + 1, sd = fd % C::kSlots;
+        if (!wait_bounded(&bar->ring_full[sd], (fd / C::kSlots) & 1, ctx, kSiteBwdDo)) break;
         if (it > 0 && !wait_bounded(&bar->dq_free, (it - 1) & 1, ctx, kSiteBwdDqFree)) break;
         tc_fence_after();
         const uint64_t dodesc = sdesc_sw128(ring + sd * C::kTileBytes, 16, 1024);
@@ -255,14 +314,33 @@ __global__ void __launch_bounds__(320, 1)
           mma_bf16_ss(tDP, vdesc + off, dodesc + off, id_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar->dp_full);
-        // ---- P^T (TMEM) and dS^T (smem) are ready
+      }
+      mma_commit(&bar->drain[0]);
+      wait_drain(&bar->drain[0], 0, kDrainLimitNs);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------------ issuer B: dV, dK, dQ
+    if (lane == 0) {
+      constexpr uint32_t id_v = idesc_bf16_f32(128, D, false, true);  // dV (A = P^T in TMEM), dK
+      constexpr uint32_t id_q = idesc_bf16_f32(128, D, true, true);   // dQ (A = dS, M-major)
+      const uint32_t ring = smem_u32(sRing);
+      const uint64_t kdesc_mn = sdesc_sw128(smem_u32(sK), 16384, 1024);
+      const uint64_t dsdesc_k = sdesc_sw128(smem_u32(sDS), 16, 1024);
+      const uint64_t dsdesc_mn = sdesc_sw128(smem_u32(sDS), 16384, 1024);
+      const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDpCol;
+      const uint32_t tDK = tmem + C::kDkCol, tDV = tmem + C::kDvCol;
+      bool ok = true;
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int sq = (2 * it) % C::kSlots, sd = (2 * it + 1) % C::kSlots;
         if (!wait_bounded(&bar->ew_done, it & 1, ctx, kSiteBwdEw)) break;
         tc_fence_after();
-        // dV += P^T dO_i
+        // dV += P^T dO_i: P^T of query group kk sits at S^T column 16 kk
         const uint64_t dodesc_mn = sdesc_sw128(ring + sd * C::kTileBytes, 16384, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tDV, tS + kk * 8, dodesc_mn + (uint32_t)((kk * 2048) >> 4), id_v, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tDV, tS + kk * 16, dodesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
+                      (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bar->dv_done);
         mma_commit(&bar->ring_empty[sd]);
         // dK += dS^T Q_i
@@ -280,58 +358,78 @@ __global__ void __launch_bounds__(320, 1)
           mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4), id_q,
                       kk > 0 ? 1u : 0u);
         mma_commit(&bar->dq_full);
-        cons += 2;
       }
       mma_commit(&bar->acc_done);
-      mma_commit(&bar->drain);
-      wait_drain(&bar->drain, 0, kDrainLimitNs);
+      mma_commit(&bar->drain[1]);
+      wait_drain(&bar->drain[1], 0, kDrainLimitNs);
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------------ elementwise + dQ read-out
-    const int g = warp >> 2;
+  } else if (warp >= 11) {
+    // ------------------------------------------------------------------ dQ warpgroup
+    // thread = query row; each warp adds its 32 rows x 32 columns per step into
+    // the fp32 accumulator with one TMA reduce-add from its own 4 KB staging tile
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // key row (elementwise) / query row (dQ read-out)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + C::kSCol + lane_off;
     const uint32_t tDP = tmem + C::kDpCol + lane_off;
-    const float sl2 = p.scale_log2;
-    constexpr float kLog2e = 1.4426950408889634f;
-    uint8_t* ds_row = sDS + g * 16384 + r * 128;
+    uint8_t* stage = sStage + (warp - 11) * 4096;
+    uint8_t* stage_row = stage + lane * 128;
     bool alive = true;
     for (int it = 0; alive && it < n_it; ++it) {
-      const int i = i_start + it;
-      const int qbase = i * 128;
-      // per-query statistics of this block into shared memory (double-buffered)
-      float* stat = sRowStat + (it & 1) * 256;
-      {
-        const int qq = tid & 127;
-        const int q = qbase + qq;
-        if (tid < 128)
-          stat[qq] = (q < N) ? p.lse[(size_t)bh * N + q] * kLog2e : CUDART_INF_F;
-        else
-          stat[128 + qq] = (q < N) ? p.delta[(size_t)bh * N + q] : 0.f;
-      }
-      if (!__all_sync(0xffffffffu, wait_bounded(&bar->s_full, it & 1, ctx, kSiteBwdS))) {
+      const int qbase = (i_start + it) * 128;
+      if (!__all_sync(0xffffffffu, wait_bounded(&bar->dq_full, it & 1, ctx, kSiteBwdDq))) {
         alive = false;
         break;
       }
       tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32(tS + 64 * g, sr[0]);
-      tmem_ld32(tS + 64 * g + 32, sr[1]);
-      tmem_wait_ld();
-      reg_fence32(sr[0]);
-      reg_fence32(sr[1]);
-      // every S^T column has been read (and this block's statistics stored)
-      // before any P^T is written over S^T; a bounded barrier, not bar.sync,
-      // so that a timed-out wait elsewhere cannot strand the other warps here
-      mbar_arrive(&bar->s_read);
-      if (!__all_sync(0xffffffffu, wait_bounded(&bar->s_read, it & 1, ctx, kSiteBwdSRead))) {
-        alive = false;
-        break;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tDP + 32 * c, v);
+        tmem_wait_ld();
+        reg_fence32(v);
+        if (c == D / 32 - 1) {
+          // all of dQ_i is in registers or staged: issuer A may overwrite these columns
+          tc_fence_before();
+          mbar_arrive(&bar->dq_free);
+        }
+        // the previous reduce of this warp must have finished reading the staging tile
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16)
+          *reinterpret_cast<uint4*>(stage_row + ((c16 ^ (lane & 7)) << 4)) =
+              make_uint4(v[4 * c16], v[4 * c16 + 1], v[4 * c16 + 2], v[4 * c16 + 3]);
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&map_dqacc, stage, 32 * c, qbase + 32 * wq, bh);
+          tma_store_commit();
+        }
       }
-      if (!__all_sync(0xffffffffu, wait_bounded(&bar->dp_full, it & 1, ctx, kSiteBwdDp))) {
+    }
+    // every reduce this warp started must be complete before the kernel ends
+    if (lane == 0) tma_store_wait_all();
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ elementwise
+    const int g = warp >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // key row
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + C::kSCol + lane_off;
+    const uint32_t tDP = tmem + C::kDpCol + lane_off;
+    const float sl2 = p.scale_log2;
+    uint8_t* ds_row = sDS + g * 16384 + r * 128;
+    bool alive = true;
+    for (int it = 0; alive && it < n_it; ++it) {
+      const int i = i_start + it;
+      const int sq = (2 * it) % C::kSlots;
+      const float* stat = reinterpret_cast<const float*>(sStat + sq * C::kStatBytes);
+      bool ok = wait_bounded(&bar->s_full, it & 1, ctx, kSiteBwdS);
+      ok = ok && wait_bounded(&bar->dp_full, it & 1, ctx, kSiteBwdDp);
+      // dS^T of the previous block must have been read by dK and dQ
+      if (it > 0) ok = ok && wait_bounded(&bar->dq_full, (it - 1) & 1, ctx, kSiteBwdDsFree);
+      if (!__all_sync(0xffffffffu, ok)) {
         alive = false;
         break;
       }
@@ -340,28 +438,36 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int qc = 64 * g + 32 * ch;  // first query column of this chunk
-        uint32_t dp[32];
+        uint32_t sv[32], dp[32];
+        tmem_ld32(tS + qc, sv);
         tmem_ld32(tDP + qc, dp);
         tmem_wait_ld();
+        reg_fence32(sv);
         reg_fence32(dp);
         uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int e2 = 0; e2 < 16; ++e2) {
-          float pv[2], dsv[2];
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(stat + qc + 4 * e4);
+          const float4 d4 = *reinterpret_cast<const float4*>(stat + 128 + qc + 4 * e4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pe[4], dse[4];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = 2 * e2 + h;
-            const float lse2 = stat[qc + e];
-            const float dl = stat[128 + qc + e];
-            float pe = ex2_approx(fmaf(__uint_as_float(sr[ch][e]), sl2, -lse2));
-            if (diag && (qc + e < r)) pe = 0.f;  // key k0 + r is in the future of query qbase + qc + e
-            pv[h] = pe;
-            dsv[h] = pe * (__uint_as_float(dp[e]) - dl);
+          for (int h = 0; h < 4; ++h) {
+            const int e = 4 * e4 + h;
+            float x = ex2_approx(fmaf(__uint_as_float(sv[e]), sl2, -lv[h]));
+            if (diag && (qc + e < r)) x = 0.f;  // key k0 + r is in the future of query qbase + qc + e
+            pe[h] = x;
+            dse[h] = x * (__uint_as_float(dp[e]) - dv4[h]);
           }
-          pk[e2] = pack_bf16x2(pv[0], pv[1]);
-          dk[e2] = pack_bf16x2(dsv[0], dsv[1]);
+          pk[2 * e4] = pack_bf16x2(pe[0], pe[1]);
+          pk[2 * e4 + 1] = pack_bf16x2(pe[2], pe[3]);
+          dk[2 * e4] = pack_bf16x2(dse[0], dse[1]);
+          dk[2 * e4 + 1] = pack_bf16x2(dse[2], dse[3]);
         }
-        tmem_st16(tS + (qc >> 1), pk);
+        // P^T of query groups qc/16 and qc/16 + 1 over the first 8 of their own columns
+        tmem_st8(tS + qc, pk);
+        tmem_st8(tS + qc + 16, pk + 8);
         // dS^T row r, queries [qc, qc+32): 4 chunks of 16 B in the swizzled atom g
 #pragma unroll
         for (int c16 = 0; c16 < 4; ++c16) {
@@ -374,32 +480,6 @@ __global__ void __launch_bounds__(320, 1)
       fence_async_shared();
       tc_fence_before();
       mbar_arrive(&bar->ew_done);
-
-      // ---- dQ_i read-out: thread = query row r, columns [g D/2, (g+1) D/2)
-      if (!__all_sync(0xffffffffu, wait_bounded(&bar->dq_full, it & 1, ctx, kSiteBwdDq))) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
-      const int qg = qbase + r;
-      float* dst = p.dq_acc + ((size_t)bh * N + qg) * D + g * (D / 2);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tDP + g * (D / 2) + 32 * c, v);
-        tmem_wait_ld();
-        reg_fence32(v);
-        if (c == D / 64 - 1) {
-          tc_fence_before();
-          mbar_arrive(&bar->dq_free);
-        }
-        if (qg < N) {
-#pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4)
-            red_add_v4(dst + 32 * c + 4 * v4, __uint_as_float(v[4 * v4]), __uint_as_float(v[4 * v4 + 1]),
-                       __uint_as_float(v[4 * v4 + 2]), __uint_as_float(v[4 * v4 + 3]));
-        }
-      }
     }
     // ---- epilogue: warpgroup 0 writes dK = scale dK_acc, warpgroup 1 writes dV
     if (alive && __all_sync(0xffffffffu, wait_bounded(&bar->acc_done, 0, ctx, kSiteBwdAcc))) {
@@ -407,7 +487,7 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t tAcc = tmem + (g ? C::kDvCol : C::kDkCol) + lane_off;
       const float mul = g ? 1.f : p.scale;
       const int kg = k0 + r;
-      __nv_bfloat16* out = (g ? p.dv : p.dk) + ((size_t)bh * N + kg) * D;
+      __nv_bfloat16* out = (g ? p.dv_out : p.dk_out) + ((size_t)bh * N + kg) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];

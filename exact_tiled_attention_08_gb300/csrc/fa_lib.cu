@@ -108,18 +108,116 @@ fa_status launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
 }
 
 template <int D, bool CAUSAL>
-fa_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
-                     const fa::BwdParams& p, int BH, cudaStream_t stream) {
+fa_status launch_bwd(const CUtensorMap* maps, const fa::BwdParams& p, int BH, cudaStream_t stream) {
   using C = fa::BwdCfg<D>;
   auto kernel = fa::fa_bwd_kernel<D, CAUSAL>;
   if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
   const long long grid = (long long)p.nkb * BH;
   const TimingEvents ev = timing_events();
   if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_start, stream) != cudaSuccess) return FA_ERR_CUDA;
-  kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                                                                  maps[6], p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_stop, stream) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
+}
+
+// fp32 [rows][cols] viewed as a 2-D tensor (cols, rows); boxes of box_cols x 1, no swizzle
+bool encode_f32_rows(CUtensorMap* map, const void* ptr, int rows, int cols, int box_cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, 1};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// the fp32 dQ accumulator [B*H][N][d] as (d, N, B*H); 32 x 32 boxes, 128-byte swizzle (reduce-add target)
+bool encode_dqacc(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// workspace of fa_bwd: fp32 dQ accumulator, then delta and LSE*log2(e) padded
+// to whole 128-row blocks, each at a 256-byte boundary
+struct BwdWorkspace {
+  size_t dq_bytes, stat_bytes;
+  static BwdWorkspace of(int B, int H, int N, int d) {
+    const size_t rows = (size_t)B * H * N;
+    const size_t npad = (size_t)((N + 127) / 128) * 128;
+    BwdWorkspace w;
+    w.dq_bytes = (rows * d * sizeof(float) + 255) & ~size_t(255);
+    w.stat_bytes = ((size_t)B * H * npad * sizeof(float) + 255) & ~size_t(255);
+    return w;
+  }
+  size_t total() const { return dq_bytes + 2 * stat_bytes; }
+};
+
+// The backward pass proper, given device scratch of BwdWorkspace::total() bytes.
+fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, void* scratch, int B, int H, int N, int d, float scale, int causal,
+                  cudaStream_t stream) {
+  const int BH = B * H;
+  const int nkb = (N + 127) / 128;
+  const int npad = nkb * 128;
+  const BwdWorkspace w = BwdWorkspace::of(B, H, N, d);
+  float* dq_acc = static_cast<float*>(scratch);
+  float* delta_pad = reinterpret_cast<float*>(static_cast<char*>(scratch) + w.dq_bytes);
+  float* lse2_pad = reinterpret_cast<float*>(static_cast<char*>(scratch) + w.dq_bytes + w.stat_bytes);
+  CUtensorMap maps[7];
+  if (!encode_bhnd(&maps[0], q, BH, N, d) || !encode_bhnd(&maps[1], k, BH, N, d) ||
+      !encode_bhnd(&maps[2], v, BH, N, d) || !encode_bhnd(&maps[3], dout, BH, N, d) ||
+      !encode_f32_rows(&maps[4], lse2_pad, BH, npad, 128) || !encode_f32_rows(&maps[5], delta_pad, BH, npad, 128) ||
+      !encode_dqacc(&maps[6], dq_acc, BH, N, d))
+    return FA_ERR_CUDA;
+  // 1. delta, LSE*log2(e) (padded), dQ accumulator = 0
+  {
+    const long long padded_rows = (long long)BH * npad;
+    const long long per_block = 256 / (d / 8);
+    long long blocks = (padded_rows + per_block - 1) / per_block;
+    if (blocks > 152LL * 16) blocks = 152LL * 16;
+    if (d == 128)
+      fa::fa_bwd_prep_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, delta_pad, lse2_pad,
+          dq_acc, N, npad, padded_rows);
+    else
+      fa::fa_bwd_prep_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, delta_pad, lse2_pad,
+          dq_acc, N, npad, padded_rows);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  }
+  // 2. dK, dV and the fp32 dQ accumulation
+  fa::BwdParams p;
+  p.dk_out = static_cast<__nv_bfloat16*>(dk);
+  p.dv_out = static_cast<__nv_bfloat16*>(dv);
+  p.N = N;
+  p.nkb = nkb;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale = scale;
+  p.wait_limit_ns = wait_limit_ns();
+  p.debug_stall = g_debug_stall.load();
+  fa_status st;
+  if (d == 128)
+    st = causal ? launch_bwd<128, true>(maps, p, BH, stream) : launch_bwd<128, false>(maps, p, BH, stream);
+  else
+    st = causal ? launch_bwd<64, true>(maps, p, BH, stream) : launch_bwd<64, false>(maps, p, BH, stream);
+  if (st != FA_OK) return st;
+  // 3. dQ = scale * dQ_acc -> bf16
+  const long long n8 = (long long)BH * N * d / 8;
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  fa::fa_dq_convert_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), scale, n8);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status launch_preprocess(const void* o, const void* dout, float* delta, float* dq_acc, long long rows, int d,
@@ -201,9 +299,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (check_shape(B, H, N, d) != FA_OK) return 0;
-  const size_t rows = (size_t)B * H * N;
-  const size_t dq_bytes = (rows * d * sizeof(float) + 255) & ~size_t(255);
-  return dq_bytes + rows * sizeof(float);
+  return BwdWorkspace::of(B, H, N, d).total();
 }
 
 fa_status fa_bwd_preprocess(const void* o, const void* dout, float* delta, int B, int H, int N, int d,
@@ -226,41 +322,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
     return FA_ERR_MISALIGNED;
-  const int BH = B * H;
-  const long long rows = (long long)BH * N;
-  float* dq_acc = static_cast<float*>(workspace);
-  const size_t dq_bytes = ((size_t)rows * d * sizeof(float) + 255) & ~size_t(255);
-  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + dq_bytes);
-  CUtensorMap mq, mk, mv, mdo;
-  if (!encode_bhnd(&mq, q, BH, N, d) || !encode_bhnd(&mk, k, BH, N, d) || !encode_bhnd(&mv, v, BH, N, d) ||
-      !encode_bhnd(&mdo, dout, BH, N, d))
-    return FA_ERR_CUDA;
-  // 1. delta = rowsum(dO o O), dQ accumulator = 0
-  if ((st = launch_preprocess(o, dout, delta, dq_acc, rows, d, stream)) != FA_OK) return st;
-  // 2. dK, dV and the fp32 dQ accumulation
-  fa::BwdParams p;
-  p.lse = lse;
-  p.delta = delta;
-  p.dq_acc = dq_acc;
-  p.dk = static_cast<__nv_bfloat16*>(dk);
-  p.dv = static_cast<__nv_bfloat16*>(dv);
-  p.N = N;
-  p.nkb = (N + 127) / 128;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.scale = scale;
-  p.wait_limit_ns = wait_limit_ns();
-  p.debug_stall = g_debug_stall.load();
-  if (d == 128)
-    st = causal ? launch_bwd<128, true>(mq, mk, mv, mdo, p, BH, stream) : launch_bwd<128, false>(mq, mk, mv, mdo, p, BH, stream);
-  else
-    st = causal ? launch_bwd<64, true>(mq, mk, mv, mdo, p, BH, stream) : launch_bwd<64, false>(mq, mk, mv, mdo, p, BH, stream);
-  if (st != FA_OK) return st;
-  // 3. dQ = scale * dQ_acc -> bf16
-  const long long n8 = rows * d / 8;
-  long long blocks = (n8 + 255) / 256;
-  if (blocks > 152LL * 16) blocks = 152LL * 16;
-  fa::fa_dq_convert_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), scale, n8);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, H, N, d, scale, causal, stream);
 }
 
 }  // extern "C"
@@ -320,41 +382,9 @@ fa_status fa_bwd_static_scratch(const void* q, const void* k, const void* v, con
     return FA_ERR_MISALIGNED;
   void* scratch = nullptr;
   if ((st = static_scratch_on_current_device(&scratch)) != FA_OK) return st;
-  const int BH = B * H;
-  const long long rows = (long long)BH * N;
-  // same layout as fa_bwd's workspace: fp32 dQ accumulator, then delta
-  float* dq_acc = static_cast<float*>(scratch);
-  const size_t dq_bytes = ((size_t)rows * d * sizeof(float) + 255) & ~size_t(255);
-  float* delta = reinterpret_cast<float*>(static_cast<char*>(scratch) + dq_bytes);
-  CUtensorMap mq, mk, mv, mdo;
-  if (!encode_bhnd(&mq, q, BH, N, d) || !encode_bhnd(&mk, k, BH, N, d) || !encode_bhnd(&mv, v, BH, N, d) ||
-      !encode_bhnd(&mdo, dout, BH, N, d))
-    return FA_ERR_CUDA;
   // the previous call's contents stay in the array: the preprocess rewrites
-  // delta and zeroes the dQ accumulator before anything reads them
-  if ((st = launch_preprocess(o, dout, delta, dq_acc, rows, d, stream)) != FA_OK) return st;
-  fa::BwdParams p;
-  p.lse = lse;
-  p.delta = delta;
-  p.dq_acc = dq_acc;
-  p.dk = static_cast<__nv_bfloat16*>(dk);
-  p.dv = static_cast<__nv_bfloat16*>(dv);
-  p.N = N;
-  p.nkb = (N + 127) / 128;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.scale = scale;
-  p.wait_limit_ns = wait_limit_ns();
-  p.debug_stall = g_debug_stall.load();
-  if (d == 128)
-    st = causal ? launch_bwd<128, true>(mq, mk, mv, mdo, p, BH, stream) : launch_bwd<128, false>(mq, mk, mv, mdo, p, BH, stream);
-  else
-    st = causal ? launch_bwd<64, true>(mq, mk, mv, mdo, p, BH, stream) : launch_bwd<64, false>(mq, mk, mv, mdo, p, BH, stream);
-  if (st != FA_OK) return st;
-  const long long n8 = rows * d / 8;
-  long long blocks = (n8 + 255) / 256;
-  if (blocks > 152LL * 16) blocks = 152LL * 16;
-  fa::fa_dq_convert_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), scale, n8);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  // delta and LSE*log2(e) and zeroes the dQ accumulator before anything reads them
+  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch, B, H, N, d, scale, causal, stream);
 }
 
 }  // extern "C"

@@ -92,7 +92,8 @@ fa_status fa_bwd_preprocess(const void* o, const void* dout, float* delta, int B
 
 /*
  * Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator
- * [B][H][N][d] followed (at a 256-byte boundary) by delta [B][H][N].
+ * [B][H][N][d], then delta and LSE*log2(e) as fp32 [B][H][Npad] each, where
+ * Npad = 128 * ceil(N / 128) (every part starting on a 256-byte boundary).
  * Returns 0 for sizes fa_bwd would reject.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
@@ -132,8 +133,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * cudaFree, no allocating library routine).
  *
  * Limit: shapes whose fa_bwd_workspace_bytes(B, H, N, d) exceeds
- * FA_STATIC_SCRATCH_BYTES (72 MiB; e.g. B*H*N*(d+1)*4 bytes must fit, as for
- * B=4, H=16, N=2048, d=128) return FA_ERR_INVALID_ARG and run nothing.
+ * FA_STATIC_SCRATCH_BYTES (72 MiB; roughly B*H*N*(d+2)*4 bytes must fit, as
+ * for B=4, H=16, N=2048, d=128) return FA_ERR_INVALID_ARG and run nothing.
  * Set-up: the first call on a device looks up the array's device address on
  * that device (cudaGetSymbolAddress, with that device current) and caches it;
  * make that first call outside any stream capture.  Sharing: every call uses

@@ -100,9 +100,12 @@ def test_preprocess_validation(lib):
 
 @pytest.mark.parametrize("B,H,N,d", [(1, 1, 128, 128), (2, 3, 1000, 64), (1, 8, 32768, 128), (16, 16, 1024, 64)])
 def test_workspace_bytes(lib, B, H, N, d):
+    # fp32 dQ accumulator, then delta and LSE*log2(e) padded to whole 128-row blocks
     rows = B * H * N
+    npad = (N + 127) // 128 * 128
     dq = (rows * d * 4 + 255) // 256 * 256
-    assert lib.fa_bwd_workspace_bytes(B, H, N, d) == dq + rows * 4
+    stat = (B * H * npad * 4 + 255) // 256 * 256
+    assert lib.fa_bwd_workspace_bytes(B, H, N, d) == dq + 2 * stat
 
 
 def test_workspace_bytes_rejects_bad_shapes(lib):
