@@ -122,8 +122,7 @@ __global__ void __launch_bounds__(256)
 //   P^T  = 2^(S^T scale log2e - LSE_i log2e), masked on the causal diagonal,
 //   dS^T = P^T o (dP^T - delta_i)                  (elementwise warps, thread = key)
 //   dV  += P^T dO_i, dK += dS^T Q_i, dQ_i = dS K_j  (issuer B)
-// and the dQ warpgroup adds dQ_i into the fp32 accumulator in global memory
-// with TMA bulk reduce-adds.  dK, dV accumulate in TMEM across all query
+// and the dQ warpgroup adds dQ_i into the fp32 accumulator in global memory.  dK, dV accumulate in TMEM across all query
 // blocks and are written once at the end.
 //
 // Warp roles (480 threads):
@@ -131,7 +130,12 @@ __global__ void __launch_bounds__(256)
 //   warp  8     issuer A (S^T, dP^T) and TMEM owner
 //   warp  9     TMA producer
 //   warp  10    issuer B (dV, dK, dQ)
-//   warps 11-14 dQ warpgroup: TMEM -> shared staging -> TMA reduce-add
+//   warps 11-14 dQ warpgroup: each warp moves its 32 query rows of dQ_i from
+//               TMEM through a 4 KB shared tile, transposes them so that 8
+//               lanes cover one 128-byte row segment, and adds them into the
+//               accumulator with red.global.add.v4.f32 (four whole lines per
+//               instruction).  Two register buffers let it release the TMEM
+//               columns after two of the d/32 chunks have gone out.
 // Tensor memory: dK at column 0, dV at d, S^T at 2d, dP^T at 2d + 128.  The
 // bf16 P^T of query group G (queries 16G..16G+15) is written over the first 8
 // of that group's own S^T columns, which only the writing thread has read;
@@ -164,6 +168,7 @@ struct BwdBarriers {
 };
 
 struct BwdParams {
+  float* dq_acc;  // [B*H][N][d] fp32, zeroed by the preprocess
   __nv_bfloat16* dk_out;
   __nv_bfloat16* dv_out;
   int N;
@@ -182,7 +187,7 @@ __global__ void __launch_bounds__(480, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                   const __grid_constant__ CUtensorMap map_lse2, const __grid_constant__ CUtensorMap map_delta,
-                  const __grid_constant__ CUtensorMap map_dqacc, const BwdParams p) {
+                  const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -238,7 +243,6 @@ __global__ void __launch_bounds__(480, 1)
   tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
   const WaitCtx ctx{&bar->abort_flag, p.wait_limit_ns};
-
   if (warp == 9) {
     // ------------------------------------------------------------------ TMA producer
     // ring fills: Q_i (with its LSE*log2e and delta rows) at 2 it, dO_i at 2 it + 1
@@ -366,50 +370,62 @@ __global__ void __launch_bounds__(480, 1)
     __syncwarp();
   } else if (warp >= 11) {
     // ------------------------------------------------------------------ dQ warpgroup
-    // thread = query row; each warp adds its 32 rows x 32 columns per step into
-    // the fp32 accumulator with one TMA reduce-add from its own 4 KB staging tile
     const int wq = warp & 3;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tDP = tmem + C::kDpCol + lane_off;
     uint8_t* stage = sStage + (warp - 11) * 4096;
-    uint8_t* stage_row = stage + lane * 128;
     bool alive = true;
     for (int it = 0; alive && it < n_it; ++it) {
-      const int qbase = (i_start + it) * 128;
+      const int qrow0 = (i_start + it) * 128 + 32 * wq;  // first query row of this warp
       if (!__all_sync(0xffffffffu, wait_bounded(&bar->dq_full, it & 1, ctx, kSiteBwdDq))) {
         alive = false;
         break;
       }
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tDP + 32 * c, v);
-        tmem_wait_ld();
-        reg_fence32(v);
-        if (c == D / 32 - 1) {
-          // all of dQ_i is in registers or staged: issuer A may overwrite these columns
-          tc_fence_before();
-          mbar_arrive(&bar->dq_free);
-        }
-        // the previous reduce of this warp must have finished reading the staging tile
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
+      // chunk c of 32 columns: row `lane` -> swizzled staging -> 8 lanes per row -> reductions
+      auto push = [&](const uint32_t(&vc)[32], int c) {
 #pragma unroll
         for (int c16 = 0; c16 < 8; ++c16)
-          *reinterpret_cast<uint4*>(stage_row + ((c16 ^ (lane & 7)) << 4)) =
-              make_uint4(v[4 * c16], v[4 * c16 + 1], v[4 * c16 + 2], v[4 * c16 + 3]);
-        fence_async_shared();
+          *reinterpret_cast<uint4*>(stage + lane * 128 + ((c16 ^ (lane & 7)) << 4)) =
+              make_uint4(vc[4 * c16], vc[4 * c16 + 1], vc[4 * c16 + 2], vc[4 * c16 + 3]);
         __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_3d(&map_dqacc, stage, 32 * c, qbase + 32 * wq, bh);
-          tma_store_commit();
+        const int chunk = lane & 7;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int row = 4 * k + (lane >> 3);
+          const float4 x = *reinterpret_cast<const float4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4));
+          if (qrow0 + row < N)
+            red_add_v4(p.dq_acc + ((size_t)bh * N + qrow0 + row) * D + 32 * c + 4 * chunk, x.x, x.y, x.z, x.w);
         }
+        __syncwarp();
+      };
+      uint32_t va[32], vb[32];
+      tmem_ld32(tDP, va);
+      tmem_ld32(tDP + 32, vb);
+      tmem_wait_ld();
+      reg_fence32(va);
+      reg_fence32(vb);
+      if constexpr (D == 64) {
+        tc_fence_before();
+        mbar_arrive(&bar->dq_free);
+        push(va, 0);
+        push(vb, 1);
+      } else {
+        push(va, 0);
+        tmem_ld32(tDP + 64, va);
+        tmem_wait_ld();
+        reg_fence32(va);
+        push(vb, 1);
+        tmem_ld32(tDP + 96, vb);
+        tmem_wait_ld();
+        reg_fence32(vb);
+        // all of dQ_i is out of TMEM: issuer A may overwrite these columns
+        tc_fence_before();
+        mbar_arrive(&bar->dq_free);
+        push(va, 2);
+        push(vb, 3);
       }
     }
-    // every reduce this warp started must be complete before the kernel ends
-    if (lane == 0) tma_store_wait_all();
-    __syncwarp();
   } else {
     // ------------------------------------------------------------------ elementwise
     const int g = warp >> 2;

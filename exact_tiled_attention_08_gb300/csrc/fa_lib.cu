@@ -116,7 +116,7 @@ fa_status launch_bwd(const CUtensorMap* maps, const fa::BwdParams& p, int BH, cu
   const TimingEvents ev = timing_events();
   if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_start, stream) != cudaSuccess) return FA_ERR_CUDA;
   kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                                                                  maps[6], p);
+                                                                  p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_stop, stream) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
@@ -132,19 +132,6 @@ bool encode_f32_rows(CUtensorMap* map, const void* ptr, int rows, int cols, int 
   const cuuint32_t elem[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, elem,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// the fp32 dQ accumulator [B*H][N][d] as (d, N, B*H); 32 x 32 boxes, 128-byte swizzle (reduce-add target)
-bool encode_dqacc(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-  const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
-  const cuuint32_t box[3] = {32, 32, 1};
-  const cuuint32_t elem[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, elem,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -174,11 +161,10 @@ fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, co
   float* dq_acc = static_cast<float*>(scratch);
   float* delta_pad = reinterpret_cast<float*>(static_cast<char*>(scratch) + w.dq_bytes);
   float* lse2_pad = reinterpret_cast<float*>(static_cast<char*>(scratch) + w.dq_bytes + w.stat_bytes);
-  CUtensorMap maps[7];
+  CUtensorMap maps[6];
   if (!encode_bhnd(&maps[0], q, BH, N, d) || !encode_bhnd(&maps[1], k, BH, N, d) ||
       !encode_bhnd(&maps[2], v, BH, N, d) || !encode_bhnd(&maps[3], dout, BH, N, d) ||
-      !encode_f32_rows(&maps[4], lse2_pad, BH, npad, 128) || !encode_f32_rows(&maps[5], delta_pad, BH, npad, 128) ||
-      !encode_dqacc(&maps[6], dq_acc, BH, N, d))
+      !encode_f32_rows(&maps[4], lse2_pad, BH, npad, 128) || !encode_f32_rows(&maps[5], delta_pad, BH, npad, 128))
     return FA_ERR_CUDA;
   // 1. delta, LSE*log2(e) (padded), dQ accumulator = 0
   {
@@ -198,6 +184,7 @@ fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, co
   }
   // 2. dK, dV and the fp32 dQ accumulation
   fa::BwdParams p;
+  p.dq_acc = dq_acc;
   p.dk_out = static_cast<__nv_bfloat16*>(dk);
   p.dv_out = static_cast<__nv_bfloat16*>(dv);
   p.N = N;
