@@ -118,24 +118,26 @@ __global__ void __launch_bounds__(256)
 // them, or i >= j when causal) stream Q_i (with its rows' LSE log2(e) and
 // delta) and dO_i through a ring.  Per query block, in the transposed
 // orientation (TMEM lane = key, column = query):
-//   S^T  = K_j Q_i^T, dP^T = V_j dO_i^T          (issuer A)
+//   dP^T = V_j dO_i^T, S^T = K_j Q_i^T          (issuer A)
 //   P^T  = 2^(S^T scale log2e - LSE_i log2e), masked on the causal diagonal,
 //   dS^T = P^T o (dP^T - delta_i)                  (elementwise warps, thread = key)
-//   dV  += P^T dO_i, dK += dS^T Q_i, dQ_i = dS K_j  (issuer B)
-// and the dQ warpgroup adds dQ_i into the fp32 accumulator in global memory.  dK, dV accumulate in TMEM across all query
+//   dK += dS^T Q_i, dQ_i = dS K_j, dV += P^T dO_i  (issuer B)
+// and the elementwise warps then add dQ_i into the fp32 accumulator in global
+// memory.  dK, dV accumulate in TMEM across all query
 // blocks and are written once at the end.
 //
-// Warp roles (480 threads):
+// Warp roles (352 threads):
 //   warps 0-7   elementwise: warpgroup g owns query columns [64 g, 64 g + 64)
-//   warp  8     issuer A (S^T, dP^T) and TMEM owner
+//               of dS, and afterwards columns [g d/2, (g+1) d/2) of dQ_i: each
+//               warp takes its 32 query rows of them out of TMEM (which frees
+//               the columns for the next dP^T at once), transposes them
+//               through its own 4 KB of the dS^T tile (free once dK and dQ
+//               have read it) so that 8 lanes cover one 128-byte row segment,
+//               and adds them with red.global.add.v4.f32, four whole lines per
+//               instruction.
+//   warp  8     issuer A (dP^T, S^T) and TMEM owner
 //   warp  9     TMA producer
-//   warp  10    issuer B (dV, dK, dQ)
-//   warps 11-14 dQ warpgroup: each warp moves its 32 query rows of dQ_i from
-//               TMEM through a 4 KB shared tile, transposes them so that 8
-//               lanes cover one 128-byte row segment, and adds them into the
-//               accumulator with red.global.add.v4.f32 (four whole lines per
-//               instruction).  Two register buffers let it release the TMEM
-//               columns after two of the d/32 chunks have gone out.
+//   warp  10    issuer B (dK, dQ, dV)
 // Tensor memory: dK at column 0, dV at d, S^T at 2d, dP^T at 2d + 128.  The
 // bf16 P^T of query group G (queries 16G..16G+15) is written over the first 8
 // of that group's own S^T columns, which only the writing thread has read;
@@ -145,15 +147,18 @@ template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kAtoms = D / 64;
-  static constexpr int kSlots = (D == 128) ? 3 : 6;   // Q / dO ring
+  static constexpr int kSlots = (D == 128) ? 4 : 6;   // Q / dO ring
   static constexpr int kStatBytes = 1024;             // LSE*log2e and delta of one query block
+  static constexpr int kStatEntries = kSlots / 2;     // one per Q tile the ring can hold
   static constexpr int kDsBytes = 128 * 128 * 2;      // dS^T tile: 2 atom columns of 64 queries
-  static constexpr int kStageBytes = 4 * 4096;        // dQ staging: 32 rows x 32 fp32 per dQ warp
-  static constexpr int kThreads = 480;
+  static constexpr int kThreads = 352;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kDkCol = 0, kDvCol = D, kSCol = 2 * D, kDpCol = 2 * D + 128;
+  // no alignment slack: the dynamic shared memory is declared 1024-byte aligned
+  // (checked at run time); at d = 128 this is 231680 of the 232448 bytes a
+  // block may have
   static constexpr int kSmemBytes =
-      1024 + 2 * kTileBytes + kSlots * kTileBytes + kDsBytes + kStageBytes + kSlots * kStatBytes + 512;
+      2 * kTileBytes + kSlots * kTileBytes + kDsBytes + kStatEntries * kStatBytes + 256;
 };
 
 struct BwdBarriers {
@@ -180,24 +185,29 @@ struct BwdParams {
 };
 
 enum : int { kSiteBwdProducer = 16, kSiteBwdKV, kSiteBwdQ, kSiteBwdDo, kSiteBwdDvDone, kSiteBwdDqFree, kSiteBwdEw,
-             kSiteBwdS, kSiteBwdDp, kSiteBwdDq, kSiteBwdAcc, kSiteBwdDsFree };
+             kSiteBwdS, kSiteBwdDp, kSiteBwdDq, kSiteBwdAcc };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(480, 1)
+__global__ void __launch_bounds__(352, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                   const __grid_constant__ CUtensorMap map_lse2, const __grid_constant__ CUtensorMap map_delta,
                   const BwdParams p) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    // the 128-byte-swizzled tiles need 1024-byte alignment: report, do nothing
+    if (threadIdx.x == 0) atomicCAS(&g_fa_device_status, 0u, kStatusBadSmem);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::kTileBytes;
   uint8_t* sRing = smem + 2 * C::kTileBytes;
   uint8_t* sDS = sRing + C::kSlots * C::kTileBytes;
-  uint8_t* sStage = sDS + C::kDsBytes;
-  uint8_t* sStat = sStage + C::kStageBytes;  // per ring slot: LSE*log2e [128] then delta [128]
-  BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(sStat + C::kSlots * C::kStatBytes);
+  // query block it: entry it % kStatEntries = LSE*log2e [128], delta [128]
+  uint8_t* sStat = sDS + C::kDsBytes;
+  BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(sStat + C::kStatEntries * C::kStatBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N;
@@ -218,7 +228,7 @@ __global__ void __launch_bounds__(480, 1)
     mbar_init(&bar->ew_done, 256);
     mbar_init(&bar->dv_done, 1);
     mbar_init(&bar->dq_full, 1);
-    mbar_init(&bar->dq_free, 128);
+    mbar_init(&bar->dq_free, 256);
     mbar_init(&bar->acc_done, 1);
     mbar_init(&bar->drain[0], 1);
     mbar_init(&bar->drain[1], 1);
@@ -268,8 +278,12 @@ __global__ void __launch_bounds__(480, 1)
           for (int a = 0; a < C::kAtoms; ++a)
             tma_load_3d(sRing + s * C::kTileBytes + a * 16384, map, &bar->ring_full[s], a * 64, i * 128, bh);
           if (!which) {
-            tma_load_2d(sStat + s * C::kStatBytes, &map_lse2, &bar->ring_full[s], i * 128, bh);
-            tma_load_2d(sStat + s * C::kStatBytes + 512, &map_delta, &bar->ring_full[s], i * 128, bh);
+            // this fill reuses the Q slot of block it - kStatEntries, which
+            // is released only after that block's elementwise step has read
+            // the same statistics entry
+            uint8_t* st = sStat + (it % C::kStatEntries) * C::kStatBytes;
+            tma_load_2d(st, &map_lse2, &bar->ring_full[s], i * 128, bh);
+            tma_load_2d(st + 512, &map_delta, &bar->ring_full[s], i * 128, bh);
           }
           ++fill;
         }
@@ -294,6 +308,18 @@ __global__ void __launch_bounds__(480, 1)
       bool ok = !(p.debug_stall && !wait_bounded(&bar->never, 0, ctx, kSiteStall));
       ok = ok && wait_bounded(&bar->kv_full, 0, ctx, kSiteBwdKV);
       for (int it = 0; ok && it < n_it; ++it) {
+        // dP^T = V dO_i^T, once the previous dQ has been taken out of these columns
+        const int fd = 2 * it + 1, sd = fd % C::kSlots;
+        if (!wait_bounded(&bar->ring_full[sd], (fd / C::kSlots) & 1, ctx, kSiteBwdDo)) break;
+        if (it > 0 && !wait_bounded(&bar->dq_free, (it - 1) & 1, ctx, kSiteBwdDqFree)) break;
+        tc_fence_after();
+        const uint64_t dodesc = sdesc_sw128(ring + sd * C::kTileBytes, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tDP, vdesc + off, dodesc + off, id_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar->dp_full);
         // S^T = K Q_i^T, once dV has consumed the previous P^T held in these columns
         const int fq = 2 * it, sq = fq % C::kSlots;
         if (!wait_bounded(&bar->ring_full[sq], (fq / C::kSlots) & 1, ctx, kSiteBwdQ)) break;
@@ -306,18 +332,6 @@ __global__ void __launch_bounds__(480, 1)
           mma_bf16_ss(tS, kdesc + off, qdesc + off, id_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar->s_full);
-        // dP^T = V dO_i^T, once the previous dQ has been read out of these columns
-        const int fd = 2 * it + 1, sd = fd % C::kSlots;
-        if (!wait_bounded(&bar->ring_full[sd], (fd / C::kSlots) & 1, ctx, kSiteBwdDo)) break;
-        if (it > 0 && !wait_bounded(&bar->dq_free, (it - 1) & 1, ctx, kSiteBwdDqFree)) break;
-        tc_fence_after();
-        const uint64_t dodesc = sdesc_sw128(ring + sd * C::kTileBytes, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tDP, vdesc + off, dodesc + off, id_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bar->dp_full);
       }
       mma_commit(&bar->drain[0]);
       wait_drain(&bar->drain[0], 0, kDrainLimitNs);
@@ -339,14 +353,6 @@ __global__ void __launch_bounds__(480, 1)
         const int sq = (2 * it) % C::kSlots, sd = (2 * it + 1) % C::kSlots;
         if (!wait_bounded(&bar->ew_done, it & 1, ctx, kSiteBwdEw)) break;
         tc_fence_after();
-        // dV += P^T dO_i: P^T of query group kk sits at S^T column 16 kk
-        const uint64_t dodesc_mn = sdesc_sw128(ring + sd * C::kTileBytes, 16384, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tDV, tS + kk * 16, dodesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
-                      (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar->dv_done);
-        mma_commit(&bar->ring_empty[sd]);
         // dK += dS^T Q_i
         const uint64_t qdesc_mn = sdesc_sw128(ring + sq * C::kTileBytes, 16384, 1024);
 #pragma unroll
@@ -355,77 +361,28 @@ __global__ void __launch_bounds__(480, 1)
           mma_bf16_ss(tDK, dsdesc_k + off, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
                       (it > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&bar->ring_empty[sq]);
-        // dQ_i = dS K
+        // dQ_i = dS K (into the dP^T columns, all read by now)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4), id_q,
                       kk > 0 ? 1u : 0u);
+        // dQ_i is ready, dS^T and Q_i have been read
         mma_commit(&bar->dq_full);
+        mma_commit(&bar->ring_empty[sq]);
+        // dV += P^T dO_i: P^T of query group kk sits at S^T column 16 kk
+        const uint64_t dodesc_mn = sdesc_sw128(ring + sd * C::kTileBytes, 16384, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tDV, tS + kk * 16, dodesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
+                      (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar->dv_done);
+        mma_commit(&bar->ring_empty[sd]);
       }
       mma_commit(&bar->acc_done);
       mma_commit(&bar->drain[1]);
       wait_drain(&bar->drain[1], 0, kDrainLimitNs);
     }
     __syncwarp();
-  } else if (warp >= 11) {
-    // ------------------------------------------------------------------ dQ warpgroup
-    const int wq = warp & 3;
-    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tDP = tmem + C::kDpCol + lane_off;
-    uint8_t* stage = sStage + (warp - 11) * 4096;
-    bool alive = true;
-    for (int it = 0; alive && it < n_it; ++it) {
-      const int qrow0 = (i_start + it) * 128 + 32 * wq;  // first query row of this warp
-      if (!__all_sync(0xffffffffu, wait_bounded(&bar->dq_full, it & 1, ctx, kSiteBwdDq))) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
-      // chunk c of 32 columns: row `lane` -> swizzled staging -> 8 lanes per row -> reductions
-      auto push = [&](const uint32_t(&vc)[32], int c) {
-#pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16)
-          *reinterpret_cast<uint4*>(stage + lane * 128 + ((c16 ^ (lane & 7)) << 4)) =
-              make_uint4(vc[4 * c16], vc[4 * c16 + 1], vc[4 * c16 + 2], vc[4 * c16 + 3]);
-        __syncwarp();
-        const int chunk = lane & 7;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int row = 4 * k + (lane >> 3);
-          const float4 x = *reinterpret_cast<const float4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4));
-          if (qrow0 + row < N)
-            red_add_v4(p.dq_acc + ((size_t)bh * N + qrow0 + row) * D + 32 * c + 4 * chunk, x.x, x.y, x.z, x.w);
-        }
-        __syncwarp();
-      };
-      uint32_t va[32], vb[32];
-      tmem_ld32(tDP, va);
-      tmem_ld32(tDP + 32, vb);
-      tmem_wait_ld();
-      reg_fence32(va);
-      reg_fence32(vb);
-      if constexpr (D == 64) {
-        tc_fence_before();
-        mbar_arrive(&bar->dq_free);
-        push(va, 0);
-        push(vb, 1);
-      } else {
-        push(va, 0);
-        tmem_ld32(tDP + 64, va);
-        tmem_wait_ld();
-        reg_fence32(va);
-        push(vb, 1);
-        tmem_ld32(tDP + 96, vb);
-        tmem_wait_ld();
-        reg_fence32(vb);
-        // all of dQ_i is out of TMEM: issuer A may overwrite these columns
-        tc_fence_before();
-        mbar_arrive(&bar->dq_free);
-        push(va, 2);
-        push(vb, 3);
-      }
-    }
   } else {
     // ------------------------------------------------------------------ elementwise
     const int g = warp >> 2;
@@ -439,12 +396,10 @@ __global__ void __launch_bounds__(480, 1)
     bool alive = true;
     for (int it = 0; alive && it < n_it; ++it) {
       const int i = i_start + it;
-      const int sq = (2 * it) % C::kSlots;
-      const float* stat = reinterpret_cast<const float*>(sStat + sq * C::kStatBytes);
+      const float* stat = reinterpret_cast<const float*>(sStat + (it % C::kStatEntries) * C::kStatBytes);
+      // (dS^T of the previous block has been read: these warps saw dq_full for it)
       bool ok = wait_bounded(&bar->s_full, it & 1, ctx, kSiteBwdS);
       ok = ok && wait_bounded(&bar->dp_full, it & 1, ctx, kSiteBwdDp);
-      // dS^T of the previous block must have been read by dK and dQ
-      if (it > 0) ok = ok && wait_bounded(&bar->dq_full, (it - 1) & 1, ctx, kSiteBwdDsFree);
       if (!__all_sync(0xffffffffu, ok)) {
         alive = false;
         break;
@@ -496,6 +451,45 @@ __global__ void __launch_bounds__(480, 1)
       fence_async_shared();
       tc_fence_before();
       mbar_arrive(&bar->ew_done);
+
+      // ---- dQ_i: thread = query row r, columns [g D/2, (g+1) D/2)
+      if (!__all_sync(0xffffffffu, wait_bounded(&bar->dq_full, it & 1, ctx, kSiteBwdDq))) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      constexpr int kChunks = D / 64;  // 32-column chunks per warp
+      uint32_t dqv[kChunks][32];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) tmem_ld32(tDP + g * (D / 2) + 32 * c, dqv[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) reg_fence32(dqv[c]);
+      // dQ_i is in registers: issuer A may overwrite these columns with dP^T
+      tc_fence_before();
+      mbar_arrive(&bar->dq_free);
+      // this warp's 4 KB of the dS^T tile (rows 32 wq .. of atom column g) as a
+      // transposing stage; dK and dQ have finished reading dS^T (dq_full)
+      uint8_t* stage = sDS + g * 16384 + wq * 4096;
+      const int qrow0 = i * 128 + 32 * wq;
+      const int chunk = lane & 7;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16)
+          *reinterpret_cast<uint4*>(stage + lane * 128 + ((c16 ^ (lane & 7)) << 4)) =
+              make_uint4(dqv[c][4 * c16], dqv[c][4 * c16 + 1], dqv[c][4 * c16 + 2], dqv[c][4 * c16 + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int row = 4 * k + (lane >> 3);
+          const float4 x = *reinterpret_cast<const float4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4));
+          if (qrow0 + row < N)
+            red_add_v4(p.dq_acc + ((size_t)bh * N + qrow0 + row) * D + g * (D / 2) + 32 * c + 4 * chunk, x.x, x.y,
+                       x.z, x.w);
+        }
+        __syncwarp();
+      }
     }
     // ---- epilogue: warpgroup 0 writes dK = scale dK_acc, warpgroup 1 writes dV
     if (alive && __all_sync(0xffffffffu, wait_bounded(&bar->acc_done, 0, ctx, kSiteBwdAcc))) {

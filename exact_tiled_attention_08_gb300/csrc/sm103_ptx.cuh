@@ -80,6 +80,7 @@ struct WaitCtx {
 };
 
 constexpr unsigned int kStatusTimeout = 5u;  // FA_ERR_TIMEOUT
+constexpr unsigned int kStatusBadSmem = 4u;  // FA_ERR_CUDA: dynamic shared memory not 1024-byte aligned
 
 // Slow path of wait_bounded (kept out of line so the fast path stays small).
 __device__ __noinline__ bool wait_bounded_slow(uint64_t* bar, uint32_t parity, const WaitCtx ctx, int site) {
