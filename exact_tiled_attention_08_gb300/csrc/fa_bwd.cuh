@@ -122,43 +122,62 @@ __global__ void __launch_bounds__(256)
 //   P^T  = 2^(S^T scale log2e - LSE_i log2e), masked on the causal diagonal,
 //   dS^T = P^T o (dP^T - delta_i)                  (elementwise warps, thread = key)
 //   dK += dS^T Q_i, dQ_i = dS K_j, dV += P^T dO_i  (issuer B)
-// and the elementwise warps then add dQ_i into the fp32 accumulator in global
-// memory.  dK, dV accumulate in TMEM across all query
-// blocks and are written once at the end.
+// and the reducer warps add dQ_i into the fp32 accumulator in global memory
+// while the next query block is processed.  dK, dV accumulate in TMEM across
+// all query blocks and are written once at the end.
 //
-// Warp roles (352 threads):
+// The global fp32 reduction of dQ_i (64 KB per query block at d = 128) is
+// bound by the L2's atomic throughput, which is close to the time the rest of
+// a query block takes; it therefore runs on warps of its own that hold dQ_i in
+// registers, so that TMEM is free for the next dP^T at once and the
+// elementwise warps never wait for it.
+//
+// Warp roles (512 threads, four warpgroups; register budgets set with
+// setmaxnreg, 144 + 144 + 144 + 80 per thread = the launch's 128 x 4):
 //   warps 0-7   elementwise: warpgroup g owns query columns [64 g, 64 g + 64)
-//               of dS, and afterwards columns [g d/2, (g+1) d/2) of dQ_i: each
-//               warp takes its 32 query rows of them out of TMEM (which frees
-//               the columns for the next dP^T at once), transposes them
-//               through its own 4 KB of the dS^T tile (free once dK and dQ
-//               have read it) so that 8 lanes cover one 128-byte row segment,
-//               and adds them with red.global.add.v4.f32, four whole lines per
-//               instruction.
-//   warp  8     issuer A (dP^T, S^T) and TMEM owner
-//   warp  9     TMA producer
-//   warp  10    issuer B (dK, dQ, dV)
+//               of dS
+//   warps 8-11  reducers: warp 8 + q takes TMEM lanes 32q.. (query rows) of
+//               dQ_i into registers, releases the columns, transposes 32 x 32
+//               blocks through its own 4 KB of shared memory so that 8 lanes
+//               cover one 128-byte row segment, and adds them with
+//               red.global.add.v4.f32, four whole lines per instruction
+//   warp  12    issuer A (dP^T, S^T) and TMEM owner
+//   warp  13    TMA producer
+//   warp  14    issuer B (dK, dQ, dV)
+//   warp  15    idle
 // Tensor memory: dK at column 0, dV at d, S^T at 2d, dP^T at 2d + 128.  The
 // bf16 P^T of query group G (queries 16G..16G+15) is written over the first 8
 // of that group's own S^T columns, which only the writing thread has read;
 // dQ_i goes into the dP^T columns once the elementwise step has read them.
 // ---------------------------------------------------------------------------
+// Register budgets per thread after setmaxnreg: the elementwise and reducer
+// warpgroups take kBwdWorkRegs, the issuing/producer warpgroup keeps
+// kBwdMiscRegs.  Each SM sub-partition holds one warp of every warpgroup, so
+// 3 x 144 + 80 = 512 = 4 x 128 uses exactly the registers the block was
+// launched with (128 per thread, which the host checks before launching).
+constexpr uint32_t kBwdWorkRegs = 144, kBwdMiscRegs = 80;
+static_assert(3 * kBwdWorkRegs + kBwdMiscRegs == 4 * 128, "register split must match the launch budget");
+
 template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kAtoms = D / 64;
-  static constexpr int kSlots = (D == 128) ? 4 : 6;   // Q / dO ring
+  static constexpr int kSlots = (D == 128) ? 3 : 6;   // Q / dO ring
   static constexpr int kStatBytes = 1024;             // LSE*log2e and delta of one query block
-  static constexpr int kStatEntries = kSlots / 2;     // one per Q tile the ring can hold
+  // one entry per query block whose statistics can be in use or in flight:
+  // Q_i is loaded once the ring slot of fill 2i - kSlots is released, and by
+  // then the elementwise step of block i - (kSlots + 1) / 2 has finished
+  static constexpr int kStatEntries = (kSlots + 1) / 2;
   static constexpr int kDsBytes = 128 * 128 * 2;      // dS^T tile: 2 atom columns of 64 queries
-  static constexpr int kThreads = 352;
+  static constexpr int kStageBytes = 4 * 4096;        // reducers' transposing tiles
+  static constexpr int kThreads = 512;
+  static constexpr int kLaunchRegs = 128;             // 65536 / 512
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kDkCol = 0, kDvCol = D, kSCol = 2 * D, kDpCol = 2 * D + 128;
-  // no alignment slack: the dynamic shared memory is declared 1024-byte aligned
-  // (checked at run time); at d = 128 this is 231680 of the 232448 bytes a
-  // block may have
+  // the dynamic shared memory is declared 1024-byte aligned (checked at run
+  // time), so no alignment slack is added
   static constexpr int kSmemBytes =
-      2 * kTileBytes + kSlots * kTileBytes + kDsBytes + kStatEntries * kStatBytes + 256;
+      2 * kTileBytes + kSlots * kTileBytes + kDsBytes + kStageBytes + kStatEntries * kStatBytes + 256;
 };
 
 struct BwdBarriers {
@@ -188,7 +207,7 @@ enum : int { kSiteBwdProducer = 16, kSiteBwdKV, kSiteBwdQ, kSiteBwdDo, kSiteBwdD
              kSiteBwdS, kSiteBwdDp, kSiteBwdDq, kSiteBwdAcc };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(512, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                   const __grid_constant__ CUtensorMap map_lse2, const __grid_constant__ CUtensorMap map_delta,
@@ -205,8 +224,9 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* sV = smem + C::kTileBytes;
   uint8_t* sRing = smem + 2 * C::kTileBytes;
   uint8_t* sDS = sRing + C::kSlots * C::kTileBytes;
+  uint8_t* sStage = sDS + C::kDsBytes;
   // query block it: entry it % kStatEntries = LSE*log2e [128], delta [128]
-  uint8_t* sStat = sDS + C::kDsBytes;
+  uint8_t* sStat = sStage + C::kStageBytes;
   BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(sStat + C::kStatEntries * C::kStatBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -228,7 +248,7 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(&bar->ew_done, 256);
     mbar_init(&bar->dv_done, 1);
     mbar_init(&bar->dq_full, 1);
-    mbar_init(&bar->dq_free, 256);
+    mbar_init(&bar->dq_free, 128);
     mbar_init(&bar->acc_done, 1);
     mbar_init(&bar->drain[0], 1);
     mbar_init(&bar->drain[1], 1);
@@ -236,11 +256,11 @@ __global__ void __launch_bounds__(352, 1)
     bar->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == 12) {
     tmem_alloc(&bar->tmem_base, C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 9 && lane == 0) {
+  if (warp == 13 && lane == 0) {
     tma_prefetch_map(&map_q);
     tma_prefetch_map(&map_k);
     tma_prefetch_map(&map_v);
@@ -253,138 +273,186 @@ __global__ void __launch_bounds__(352, 1)
   tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
   const WaitCtx ctx{&bar->abort_flag, p.wait_limit_ns};
-  if (warp == 9) {
-    // ------------------------------------------------------------------ TMA producer
-    // ring fills: Q_i (with its LSE*log2e and delta rows) at 2 it, dO_i at 2 it + 1
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bar->kv_full, 2 * C::kTileBytes);
-      for (int a = 0; a < C::kAtoms; ++a) {
-        tma_load_3d(sK + a * 16384, &map_k, &bar->kv_full, a * 64, k0, bh);
-        tma_load_3d(sV + a * 16384, &map_v, &bar->kv_full, a * 64, k0, bh);
-      }
-      int fill = 0;
-      bool ok = true;
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int i = i_start + it;
-        for (int which = 0; which < 2; ++which) {
-          const int s = fill % C::kSlots;
-          const uint32_t u = fill / C::kSlots;
-          if (!wait_bounded(&bar->ring_empty[s], (u & 1) ^ 1, ctx, kSiteBwdProducer)) {
-            ok = false;
-            break;
+  if (warp >= 12) {
+    setmaxnreg_dec<kBwdMiscRegs>();
+    if (warp == 13) {
+      // ---------------------------------------------------------------- TMA producer
+      // ring fills: Q_i (with its LSE*log2e and delta rows) at 2 it, dO_i at 2 it + 1
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar->kv_full, 2 * C::kTileBytes);
+        for (int a = 0; a < C::kAtoms; ++a) {
+          tma_load_3d(sK + a * 16384, &map_k, &bar->kv_full, a * 64, k0, bh);
+          tma_load_3d(sV + a * 16384, &map_v, &bar->kv_full, a * 64, k0, bh);
+        }
+        int fill = 0;
+        bool ok = true;
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int i = i_start + it;
+          for (int which = 0; which < 2; ++which) {
+            const int s = fill % C::kSlots;
+            const uint32_t u = fill / C::kSlots;
+            if (!wait_bounded_inl(&bar->ring_empty[s], (u & 1) ^ 1, ctx, kSiteBwdProducer)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bar->ring_full[s], C::kTileBytes + (which ? 0 : C::kStatBytes));
+            const CUtensorMap* map = which ? &map_do : &map_q;
+            for (int a = 0; a < C::kAtoms; ++a)
+              tma_load_3d(sRing + s * C::kTileBytes + a * 16384, map, &bar->ring_full[s], a * 64, i * 128, bh);
+            if (!which) {
+              // the entry was last read by the elementwise step of block
+              // it - kStatEntries, which has finished once this slot is free
+              uint8_t* st = sStat + (it % C::kStatEntries) * C::kStatBytes;
+              tma_load_2d(st, &map_lse2, &bar->ring_full[s], i * 128, bh);
+              tma_load_2d(st + 512, &map_delta, &bar->ring_full[s], i * 128, bh);
+            }
+            ++fill;
           }
-          mbar_arrive_expect_tx(&bar->ring_full[s], C::kTileBytes + (which ? 0 : C::kStatBytes));
-          const CUtensorMap* map = which ? &map_do : &map_q;
-          for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_3d(sRing + s * C::kTileBytes + a * 16384, map, &bar->ring_full[s], a * 64, i * 128, bh);
-          if (!which) {
-            // this fill reuses the Q slot of block it - kStatEntries, which
-            // is released only after that block's elementwise step has read
-            // the same statistics entry
-            uint8_t* st = sStat + (it % C::kStatEntries) * C::kStatBytes;
-            tma_load_2d(st, &map_lse2, &bar->ring_full[s], i * 128, bh);
-            tma_load_2d(st + 512, &map_delta, &bar->ring_full[s], i * 128, bh);
+        }
+        wait_drain_inl(&bar->kv_full, 0, kDrainLimitNs);
+        for (int s = 0; s < C::kSlots; ++s) {
+          if (fill > s) {
+            const int uses = (fill - 1 - s) / C::kSlots + 1;
+            wait_drain_inl(&bar->ring_full[s], (uses - 1) & 1, kDrainLimitNs);
           }
-          ++fill;
         }
       }
-      wait_drain(&bar->kv_full, 0, kDrainLimitNs);
-      for (int s = 0; s < C::kSlots; ++s) {
-        if (fill > s) {
-          const int uses = (fill - 1 - s) / C::kSlots + 1;
-          wait_drain(&bar->ring_full[s], (uses - 1) & 1, kDrainLimitNs);
+      __syncwarp();
+    } else if (warp == 12) {
+      // ---------------------------------------------------------------- issuer A: dP^T, S^T
+      if (lane == 0) {
+        constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+        const uint32_t ring = smem_u32(sRing);
+        const uint64_t kdesc = sdesc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16, 1024);
+        const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDpCol;
+        bool ok = !(p.debug_stall && !wait_bounded_inl(&bar->never, 0, ctx, kSiteStall));
+        ok = ok && wait_bounded_inl(&bar->kv_full, 0, ctx, kSiteBwdKV);
+        for (int it = 0; ok && it < n_it; ++it) {
+          // dP^T = V dO_i^T, once the reducers have taken the previous dQ out of these columns
+          const int fd = 2 * it + 1, sd = fd % C::kSlots;
+          if (!wait_bounded_inl(&bar->ring_full[sd], (fd / C::kSlots) & 1, ctx, kSiteBwdDo)) break;
+          if (it > 0 && !wait_bounded_inl(&bar->dq_free, (it - 1) & 1, ctx, kSiteBwdDqFree)) break;
+          tc_fence_after();
+          const uint64_t dodesc = sdesc_sw128(ring + sd * C::kTileBytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+            mma_bf16_ss(tDP, vdesc + off, dodesc + off, id_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar->dp_full);
+          // S^T = K Q_i^T, once dV has consumed the previous P^T held in these
+          // columns (dv_done also covers the dK and dQ products issued before
+          // dV, so the dS^T tile of the previous block has been read as well)
+          const int fq = 2 * it, sq = fq % C::kSlots;
+          if (!wait_bounded_inl(&bar->ring_full[sq], (fq / C::kSlots) & 1, ctx, kSiteBwdQ)) break;
+          if (it > 0 && !wait_bounded_inl(&bar->dv_done, (it - 1) & 1, ctx, kSiteBwdDvDone)) break;
+          tc_fence_after();
+          const uint64_t qdesc = sdesc_sw128(ring + sq * C::kTileBytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+            mma_bf16_ss(tS, kdesc + off, qdesc + off, id_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar->s_full);
         }
+        mma_commit(&bar->drain[0]);
+        wait_drain_inl(&bar->drain[0], 0, kDrainLimitNs);
+      }
+      __syncwarp();
+    } else if (warp == 14) {
+      // ---------------------------------------------------------------- issuer B: dK, dQ, dV
+      if (lane == 0) {
+        constexpr uint32_t id_v = idesc_bf16_f32(128, D, false, true);  // dV (A = P^T in TMEM), dK
+        constexpr uint32_t id_q = idesc_bf16_f32(128, D, true, true);   // dQ (A = dS, M-major)
+        const uint32_t ring = smem_u32(sRing);
+        const uint64_t kdesc_mn = sdesc_sw128(smem_u32(sK), 16384, 1024);
+        const uint64_t dsdesc_k = sdesc_sw128(smem_u32(sDS), 16, 1024);
+        const uint64_t dsdesc_mn = sdesc_sw128(smem_u32(sDS), 16384, 1024);
+        const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDpCol;
+        const uint32_t tDK = tmem + C::kDkCol, tDV = tmem + C::kDvCol;
+        bool ok = true;
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int sq = (2 * it) % C::kSlots, sd = (2 * it + 1) % C::kSlots;
+          if (!wait_bounded_inl(&bar->ew_done, it & 1, ctx, kSiteBwdEw)) break;
+          tc_fence_after();
+          // dK += dS^T Q_i
+          const uint64_t qdesc_mn = sdesc_sw128(ring + sq * C::kTileBytes, 16384, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+            mma_bf16_ss(tDK, dsdesc_k + off, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
+                        (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          // Q_i has been read by S^T (long complete) and dK: release its slot
+          // now, so that the next dO tile can come in while dQ and dV run
+          mma_commit(&bar->ring_empty[sq]);
+          // dQ_i = dS K (into the dP^T columns, all read by now)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4), id_q,
+                        kk > 0 ? 1u : 0u);
+          mma_commit(&bar->dq_full);
+          // dV += P^T dO_i: P^T of query group kk sits at S^T column 16 kk
+          const uint64_t dodesc_mn = sdesc_sw128(ring + sd * C::kTileBytes, 16384, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ts(tDV, tS + kk * 16, dodesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
+                        (it > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bar->dv_done);
+          mma_commit(&bar->ring_empty[sd]);
+        }
+        mma_commit(&bar->acc_done);
+        mma_commit(&bar->drain[1]);
+        wait_drain_inl(&bar->drain[1], 0, kDrainLimitNs);
+      }
+      __syncwarp();
+    }
+    // warp 15 has no role
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------------ reducers
+    setmaxnreg_inc<kBwdWorkRegs>();
+    const int q = warp & 3;
+    const uint32_t tDQ = tmem + C::kDpCol + ((uint32_t)(q * 32) << 16);
+    uint8_t* stage = sStage + q * 4096;
+    const int chunk = lane & 7;
+    constexpr int kChunks = D / 32;  // 32-column chunks of a dQ row
+    for (int it = 0; it < n_it; ++it) {
+      if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->dq_full, it & 1, ctx, kSiteBwdDq))) break;
+      tc_fence_after();
+      uint32_t dqv[kChunks][32];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) tmem_ld32(tDQ + 32 * c, dqv[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) reg_fence32(dqv[c]);
+      // dQ_i is in registers: issuer A may overwrite these columns with dP^T
+      tc_fence_before();
+      mbar_arrive(&bar->dq_free);
+      // thread = query row 32 q + lane; each 32 x 32 block goes through the
+      // stage (row-major, 16-byte chunks swizzled by row) and comes back with
+      // 8 lanes per row, so that each reduction covers four whole 128-byte lines
+      const int qrow0 = (i_start + it) * 128 + 32 * q;
+      float* acc_rows = p.dq_acc + ((size_t)bh * N + qrow0) * D;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16)
+          *reinterpret_cast<uint4*>(stage + lane * 128 + ((c16 ^ (lane & 7)) << 4)) =
+              make_uint4(dqv[c][4 * c16], dqv[c][4 * c16 + 1], dqv[c][4 * c16 + 2], dqv[c][4 * c16 + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int row = 4 * k + (lane >> 3);
+          const float4 x = *reinterpret_cast<const float4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4));
+          if (qrow0 + row < N) red_add_v4(acc_rows + (size_t)row * D + 32 * c + 4 * chunk, x.x, x.y, x.z, x.w);
+        }
+        __syncwarp();
       }
     }
-    __syncwarp();
-  } else if (warp == 8) {
-    // ------------------------------------------------------------------ issuer A: S^T, dP^T
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-      const uint32_t ring = smem_u32(sRing);
-      const uint64_t kdesc = sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16, 1024);
-      const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDpCol;
-      bool ok = !(p.debug_stall && !wait_bounded(&bar->never, 0, ctx, kSiteStall));
-      ok = ok && wait_bounded(&bar->kv_full, 0, ctx, kSiteBwdKV);
-      for (int it = 0; ok && it < n_it; ++it) {
-        // dP^T = V dO_i^T, once the previous dQ has been taken out of these columns
-        const int fd = 2 * it + 1, sd = fd % C::kSlots;
-        if (!wait_bounded(&bar->ring_full[sd], (fd / C::kSlots) & 1, ctx, kSiteBwdDo)) break;
-        if (it > 0 && !wait_bounded(&bar->dq_free, (it - 1) & 1, ctx, kSiteBwdDqFree)) break;
-        tc_fence_after();
-        const uint64_t dodesc = sdesc_sw128(ring + sd * C::kTileBytes, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tDP, vdesc + off, dodesc + off, id_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bar->dp_full);
-        // S^T = K Q_i^T, once dV has consumed the previous P^T held in these columns
-        const int fq = 2 * it, sq = fq % C::kSlots;
-        if (!wait_bounded(&bar->ring_full[sq], (fq / C::kSlots) & 1, ctx, kSiteBwdQ)) break;
-        if (it > 0 && !wait_bounded(&bar->dv_done, (it - 1) & 1, ctx, kSiteBwdDvDone)) break;
-        tc_fence_after();
-        const uint64_t qdesc = sdesc_sw128(ring + sq * C::kTileBytes, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tS, kdesc + off, qdesc + off, id_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bar->s_full);
-      }
-      mma_commit(&bar->drain[0]);
-      wait_drain(&bar->drain[0], 0, kDrainLimitNs);
-    }
-    __syncwarp();
-  } else if (warp == 10) {
-    // ------------------------------------------------------------------ issuer B: dV, dK, dQ
-    if (lane == 0) {
-      constexpr uint32_t id_v = idesc_bf16_f32(128, D, false, true);  // dV (A = P^T in TMEM), dK
-      constexpr uint32_t id_q = idesc_bf16_f32(128, D, true, true);   // dQ (A = dS, M-major)
-      const uint32_t ring = smem_u32(sRing);
-      const uint64_t kdesc_mn = sdesc_sw128(smem_u32(sK), 16384, 1024);
-      const uint64_t dsdesc_k = sdesc_sw128(smem_u32(sDS), 16, 1024);
-      const uint64_t dsdesc_mn = sdesc_sw128(smem_u32(sDS), 16384, 1024);
-      const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDpCol;
-      const uint32_t tDK = tmem + C::kDkCol, tDV = tmem + C::kDvCol;
-      bool ok = true;
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int sq = (2 * it) % C::kSlots, sd = (2 * it + 1) % C::kSlots;
-        if (!wait_bounded(&bar->ew_done, it & 1, ctx, kSiteBwdEw)) break;
-        tc_fence_after();
-        // dK += dS^T Q_i
-        const uint64_t qdesc_mn = sdesc_sw128(ring + sq * C::kTileBytes, 16384, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tDK, dsdesc_k + off, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
-                      (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        // dQ_i = dS K (into the dP^T columns, all read by now)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4), id_q,
-                      kk > 0 ? 1u : 0u);
-        // dQ_i is ready, dS^T and Q_i have been read
-        mma_commit(&bar->dq_full);
-        mma_commit(&bar->ring_empty[sq]);
-        // dV += P^T dO_i: P^T of query group kk sits at S^T column 16 kk
-        const uint64_t dodesc_mn = sdesc_sw128(ring + sd * C::kTileBytes, 16384, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tDV, tS + kk * 16, dodesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
-                      (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar->dv_done);
-        mma_commit(&bar->ring_empty[sd]);
-      }
-      mma_commit(&bar->acc_done);
-      mma_commit(&bar->drain[1]);
-      wait_drain(&bar->drain[1], 0, kDrainLimitNs);
-    }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------------ elementwise
+    setmaxnreg_inc<kBwdWorkRegs>();
     const int g = warp >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row
@@ -397,9 +465,10 @@ __global__ void __launch_bounds__(352, 1)
     for (int it = 0; alive && it < n_it; ++it) {
       const int i = i_start + it;
       const float* stat = reinterpret_cast<const float*>(sStat + (it % C::kStatEntries) * C::kStatBytes);
-      // (dS^T of the previous block has been read: these warps saw dq_full for it)
-      bool ok = wait_bounded(&bar->s_full, it & 1, ctx, kSiteBwdS);
-      ok = ok && wait_bounded(&bar->dp_full, it & 1, ctx, kSiteBwdDp);
+      // S^T of this block was issued after dV of the previous one, which also
+      // covers its dK and dQ: the dS^T tile is free to be overwritten
+      bool ok = wait_bounded_inl(&bar->s_full, it & 1, ctx, kSiteBwdS);
+      ok = ok && wait_bounded_inl(&bar->dp_full, it & 1, ctx, kSiteBwdDp);
       if (!__all_sync(0xffffffffu, ok)) {
         alive = false;
         break;
@@ -451,48 +520,9 @@ __global__ void __launch_bounds__(352, 1)
       fence_async_shared();
       tc_fence_before();
       mbar_arrive(&bar->ew_done);
-
-      // ---- dQ_i: thread = query row r, columns [g D/2, (g+1) D/2)
-      if (!__all_sync(0xffffffffu, wait_bounded(&bar->dq_full, it & 1, ctx, kSiteBwdDq))) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
-      constexpr int kChunks = D / 64;  // 32-column chunks per warp
-      uint32_t dqv[kChunks][32];
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) tmem_ld32(tDP + g * (D / 2) + 32 * c, dqv[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) reg_fence32(dqv[c]);
-      // dQ_i is in registers: issuer A may overwrite these columns with dP^T
-      tc_fence_before();
-      mbar_arrive(&bar->dq_free);
-      // this warp's 4 KB of the dS^T tile (rows 32 wq .. of atom column g) as a
-      // transposing stage; dK and dQ have finished reading dS^T (dq_full)
-      uint8_t* stage = sDS + g * 16384 + wq * 4096;
-      const int qrow0 = i * 128 + 32 * wq;
-      const int chunk = lane & 7;
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-#pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16)
-          *reinterpret_cast<uint4*>(stage + lane * 128 + ((c16 ^ (lane & 7)) << 4)) =
-              make_uint4(dqv[c][4 * c16], dqv[c][4 * c16 + 1], dqv[c][4 * c16 + 2], dqv[c][4 * c16 + 3]);
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int row = 4 * k + (lane >> 3);
-          const float4 x = *reinterpret_cast<const float4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4));
-          if (qrow0 + row < N)
-            red_add_v4(p.dq_acc + ((size_t)bh * N + qrow0 + row) * D + g * (D / 2) + 32 * c + 4 * chunk, x.x, x.y,
-                       x.z, x.w);
-        }
-        __syncwarp();
-      }
     }
     // ---- epilogue: warpgroup 0 writes dK = scale dK_acc, warpgroup 1 writes dV
-    if (alive && __all_sync(0xffffffffu, wait_bounded(&bar->acc_done, 0, ctx, kSiteBwdAcc))) {
+    if (alive && __all_sync(0xffffffffu, wait_bounded_inl(&bar->acc_done, 0, ctx, kSiteBwdAcc))) {
       tc_fence_after();
       const uint32_t tAcc = tmem + (g ? C::kDvCol : C::kDkCol) + lane_off;
       const float mul = g ? 1.f : p.scale;
@@ -522,7 +552,7 @@ __global__ void __launch_bounds__(352, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 12) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

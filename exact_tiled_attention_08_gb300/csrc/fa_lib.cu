@@ -112,6 +112,10 @@ fa_status launch_bwd(const CUtensorMap* maps, const fa::BwdParams& p, int BH, cu
   using C = fa::BwdCfg<D>;
   auto kernel = fa::fa_bwd_kernel<D, CAUSAL>;
   if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
+  // the kernel's warpgroups re-divide the registers the block launches with
+  // (setmaxnreg); that only works if the block really gets 128 per thread
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess || attr.numRegs != C::kLaunchRegs) return FA_ERR_CUDA;
   const long long grid = (long long)p.nkb * BH;
   const TimingEvents ev = timing_events();
   if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_start, stream) != cudaSuccess) return FA_ERR_CUDA;

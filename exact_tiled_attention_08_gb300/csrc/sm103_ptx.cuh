@@ -107,6 +107,46 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, con
   return wait_bounded_slow(bar, parity, ctx, site);
 }
 
+// The same bounded wait with its slow path inlined, for warps that have
+// changed their register budget with setmaxnreg (such code cannot call a
+// function that is not inlined).
+__device__ __forceinline__ bool wait_bounded_inl(uint64_t* bar, uint32_t parity, const WaitCtx& ctx, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*ctx.abort_flag) return false;
+    if (global_timer_ns() - t0 > ctx.limit_ns) {
+      atomicCAS(&g_fa_device_status, 0u, kStatusTimeout | ((unsigned)(site & 0xff) << 8));
+      *ctx.abort_flag = 1;
+      __threadfence_block();
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_drain_inl(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// Register budget of the calling warpgroup (all of its threads execute it):
+// the block launches with a uniform count per thread, and warpgroups then
+// give registers back (dec) or take them (inc) from the block's pool.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // Wait used while draining after an abort: ignores the abort flag, gives up
 // after `limit_ns` without touching the status word.
 __device__ __noinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
