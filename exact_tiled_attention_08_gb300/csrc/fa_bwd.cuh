@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(256)
 // them, or i >= j when causal) stream Q_i (with its rows' LSE log2(e) and
 // delta) and dO_i through a ring.  Per query block, in the transposed
 // orientation (TMEM lane = key, column = query):
-//   dP^T = V_j dO_i^T, S^T = K_j Q_i^T          (issuer A)
+//   S^T = K_j Q_i^T and dP^T = V_j dO_i^T        (issuer A)
 //   P^T  = 2^(S^T scale log2e - LSE_i log2e), masked on the causal diagonal,
 //   dS^T = P^T o (dP^T - delta_i)                  (elementwise warps, thread = key)
 //   dK += dS^T Q_i, dQ_i = dS K_j, dV += P^T dO_i  (issuer B)
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(256)
 //               blocks through its own 4 KB of shared memory so that 8 lanes
 //               cover one 128-byte row segment, and adds them with
 //               red.global.add.v4.f32, four whole lines per instruction
-//   warp  12    issuer A (dP^T, S^T) and TMEM owner
+//   warp  12    issuer A (S^T and dP^T) and TMEM owner
 //   warp  13    TMA producer
 //   warp  14    issuer B (dK, dQ, dV)
 //   warp  15    idle
@@ -299,6 +299,11 @@ __global__ void __launch_bounds__(512, 1)
             const CUtensorMap* map = which ? &map_do : &map_q;
             for (int a = 0; a < C::kAtoms; ++a)
               tma_load_3d(sRing + s * C::kTileBytes + a * 16384, map, &bar->ring_full[s], a * 64, i * 128, bh);
+            // with a three-slot ring the same tile of the next query block goes
+            // to L2 now, so that its load (which waits for a free slot) is
+            // served from L2
+            if (C::kSlots < 4 && it + 1 < n_it)
+              for (int a = 0; a < C::kAtoms; ++a) tma_prefetch_l2_3d(map, a * 64, (i + 1) * 128, bh);
             if (!which) {
               // the entry was last read by the elementwise step of block
               // it - kStatEntries, which has finished once this slot is free
@@ -319,7 +324,7 @@ __global__ void __launch_bounds__(512, 1)
       }
       __syncwarp();
     } else if (warp == 12) {
-      // ---------------------------------------------------------------- issuer A: dP^T, S^T
+      // ---------------------------------------------------------------- issuer A: S^T and dP^T
       if (lane == 0) {
         constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
         const uint32_t ring = smem_u32(sRing);
@@ -328,33 +333,46 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDpCol;
         bool ok = !(p.debug_stall && !wait_bounded_inl(&bar->never, 0, ctx, kSiteStall));
         ok = ok && wait_bounded_inl(&bar->kv_full, 0, ctx, kSiteBwdKV);
+        // With a three-slot ring dO_i comes in only after dK of the previous
+        // block has released Q_{i-1}'s slot, so S^T (whose Q_i was loaded long
+        // before) goes first; with more slots dP^T goes first, since the
+        // reducers free its columns before dV completes.
+        constexpr bool kSFirst = C::kSlots < 4;
         for (int it = 0; ok && it < n_it; ++it) {
-          // dP^T = V dO_i^T, once the reducers have taken the previous dQ out of these columns
-          const int fd = 2 * it + 1, sd = fd % C::kSlots;
-          if (!wait_bounded_inl(&bar->ring_full[sd], (fd / C::kSlots) & 1, ctx, kSiteBwdDo)) break;
-          if (it > 0 && !wait_bounded_inl(&bar->dq_free, (it - 1) & 1, ctx, kSiteBwdDqFree)) break;
-          tc_fence_after();
-          const uint64_t dodesc = sdesc_sw128(ring + sd * C::kTileBytes, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-            mma_bf16_ss(tDP, vdesc + off, dodesc + off, id_s, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bar->dp_full);
-          // S^T = K Q_i^T, once dV has consumed the previous P^T held in these
-          // columns (dv_done also covers the dK and dQ products issued before
-          // dV, so the dS^T tile of the previous block has been read as well)
-          const int fq = 2 * it, sq = fq % C::kSlots;
-          if (!wait_bounded_inl(&bar->ring_full[sq], (fq / C::kSlots) & 1, ctx, kSiteBwdQ)) break;
-          if (it > 0 && !wait_bounded_inl(&bar->dv_done, (it - 1) & 1, ctx, kSiteBwdDvDone)) break;
-          tc_fence_after();
-          const uint64_t qdesc = sdesc_sw128(ring + sq * C::kTileBytes, 16, 1024);
+          for (int step = 0; step < 2; ++step) {
+            if ((step == 0) == kSFirst) {
+              // S^T = K Q_i^T, once dV has consumed the previous P^T held in
+              // these columns (dv_done also covers the dK and dQ products
+              // issued before dV, so the dS^T tile of the previous block has
+              // been read as well)
+              const int fq = 2 * it, sq = fq % C::kSlots;
+              if (!wait_bounded_inl(&bar->ring_full[sq], (fq / C::kSlots) & 1, ctx, kSiteBwdQ)) { ok = false; break; }
+              if (it > 0 && !wait_bounded_inl(&bar->dv_done, (it - 1) & 1, ctx, kSiteBwdDvDone)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t qdesc = sdesc_sw128(ring + sq * C::kTileBytes, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-            mma_bf16_ss(tS, kdesc + off, qdesc + off, id_s, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                mma_bf16_ss(tS, kdesc + off, qdesc + off, id_s, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&bar->s_full);
+            } else {
+              // dP^T = V dO_i^T, once the reducers have taken the previous dQ
+              // out of these columns
+              const int fd = 2 * it + 1, sd = fd % C::kSlots;
+              if (!wait_bounded_inl(&bar->ring_full[sd], (fd / C::kSlots) & 1, ctx, kSiteBwdDo)) { ok = false; break; }
+              if (it > 0 && !wait_bounded_inl(&bar->dq_free, (it - 1) & 1, ctx, kSiteBwdDqFree)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t dodesc = sdesc_sw128(ring + sd * C::kTileBytes, 16, 1024);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                mma_bf16_ss(tDP, vdesc + off, dodesc + off, id_s, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&bar->dp_full);
+            }
           }
-          mma_commit(&bar->s_full);
         }
         mma_commit(&bar->drain[0]);
         wait_drain_inl(&bar->drain[0], 0, kDrainLimitNs);
