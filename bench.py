@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-chunks", type=int, default=2,
+                    help="head chunks pipelined over copy-in / compute / copy-out streams in the end-to-end leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -338,32 +340,67 @@ def run_ours(args, rank, world, local):
     step_ms_max = max_over_ranks(step_ms, world)
     value = world * step_flops / (step_ms_max / 1e3) / 1e12
 
-    # ---- end to end through the C ABI with pinned host buffers
+    # ---- end to end through the C ABI with pinned host buffers.  The heads
+    # are split into chunks (every tensor is laid out head-major, so a range of
+    # heads is a contiguous slice) and pipelined over three streams: while
+    # chunk c is computed, chunk c+1's inputs come in and chunk c-1's results
+    # go out.  Each chunk is one fa_fwd + fa_bwd call on its heads.
+    o_ref = o.clone()
     h_in = {x: inp_cpu[x].pin_memory() for x in ("q", "k", "v", "do")}
     h_out = {"o": torch.empty_like(o, device="cpu").pin_memory(), "lse": torch.empty_like(lse, device="cpu").pin_memory(),
              "dq": torch.empty_like(dq, device="cpu").pin_memory(), "dk": torch.empty_like(dk, device="cpu").pin_memory(),
              "dv": torch.empty_like(dv, device="cpu").pin_memory()}
+    d_in = {"q": q, "k": k, "v": v, "do": do}
     d_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    BH = w.B * w.H
+    chunks = max(1, min(args.e2e_chunks, BH))
+    bounds = [(c * BH // chunks, (c + 1) * BH // chunks) for c in range(chunks)]
+
+    def heads(t, lo, hi):
+        # [B, H, ...] -> [1, hi - lo, ...] view of heads lo..hi-1 (contiguous)
+        return t.view(1, BH, *t.shape[2:])[:, lo:hi]
+
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     E = max(1, args.e2e_steps)
-    with torch.cuda.stream(stream):
-        e2e_ev = []
-        for i in range(E + 3):
-            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s0.record(stream)
-            q.copy_(h_in["q"], non_blocking=True)
-            k.copy_(h_in["k"], non_blocking=True)
-            v.copy_(h_in["v"], non_blocking=True)
-            do.copy_(h_in["do"], non_blocking=True)
-            step()
-            for name, t in h_out.items():
-                t.copy_(d_out[name], non_blocking=True)
-            s1.record(stream)
-            if i >= 3:
-                e2e_ev.append((s0, s1))
-        torch.cuda.synchronize(dev)
-        assert fa.fa_check_device_status(stream) == fa.FA_OK
+    e2e_ev = []
+    prev_end = None
+    for i in range(E + 3):
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if prev_end is not None:
+            s_in.wait_event(prev_end)
+        s0.record(s_in)
+        stream.wait_event(s0)
+        s_out.wait_event(s0)
+        for lo, hi in bounds:
+            with torch.cuda.stream(s_in):
+                for name, t in d_in.items():
+                    heads(t, lo, hi).copy_(heads(h_in[name], lo, hi), non_blocking=True)
+                got_in = torch.cuda.Event()
+                got_in.record(s_in)
+            stream.wait_event(got_in)
+            with torch.cuda.stream(stream):
+                qc, kc, vc, doc = (heads(d_in[x], lo, hi) for x in ("q", "k", "v", "do"))
+                oc, lc = heads(o, lo, hi), heads(lse, lo, hi)
+                fa.fa_fwd(qc, kc, vc, oc, lc, scale, w.causal, stream)
+                fa.fa_bwd(qc, kc, vc, oc, doc, lc, heads(dq, lo, hi), heads(dk, lo, hi), heads(dv, lo, hi), ws, scale,
+                          w.causal, stream)
+                done = torch.cuda.Event()
+                done.record(stream)
+            s_out.wait_event(done)
+            with torch.cuda.stream(s_out):
+                for name, t in h_out.items():
+                    heads(t, lo, hi).copy_(heads(d_out[name], lo, hi), non_blocking=True)
+        s1.record(s_out)
+        prev_end = s1
+        if i >= 3:
+            e2e_ev.append((s0, s1))
+    torch.cuda.synchronize(dev)
+    assert fa.fa_check_device_status(stream) == fa.FA_OK
+    # the pipelined run computed exactly what the device-resident one did
+    if not torch.equal(h_out["o"], o_ref.cpu()):
+        raise SystemExit("bench.py: end-to-end outputs differ from the device-resident run")
     e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), world)
     e2e_value = world * step_flops / (e2e_ms / 1e3) / 1e12
 
@@ -395,7 +432,7 @@ def run_ours(args, rank, world, local):
                       "other_ms": step_ms - fwd_ms - bwd_ms,
                       "fwd_frac_of_sustained_peak": fwd_tf / peak, "bwd_frac_of_sustained_peak": bwd_tf / peak},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms, "chunks": chunks},
         "gpu_launches": 4 * K,
         "clocks": clock_info,
     }
