@@ -503,25 +503,29 @@ __global__ void __launch_bounds__(512, 1)
         reg_fence32(sv);
         reg_fence32(dp);
         uint32_t pk[16], dk[16];
+        const float2 c2 = make_float2(sl2, sl2);
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
+          // four queries' L*log2e and delta (the same for every thread: broadcast reads)
           const float4 l4 = *reinterpret_cast<const float4*>(stat + qc + 4 * e4);
           const float4 d4 = *reinterpret_cast<const float4*>(stat + 128 + qc + 4 * e4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pe[4], dse[4];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int e = 4 * e4 + h;
-            float x = ex2_approx(fmaf(__uint_as_float(sv[e]), sl2, -lv[h]));
-            if (diag && (qc + e < r)) x = 0.f;  // key k0 + r is in the future of query qbase + qc + e
-            pe[h] = x;
-            dse[h] = x * (__uint_as_float(dp[e]) - dv4[h]);
+          for (int h = 0; h < 2; ++h) {
+            const int e = 4 * e4 + 2 * h;  // two queries at a time (packed fp32x2 arithmetic)
+            const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+            const float2 dl = h ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+            const float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nl);
+            float2 pe = make_float2(ex2_approx(xs.x), ex2_approx(xs.y));
+            if (diag) {  // key k0 + r is in the future of query qbase + qc + e
+              if (qc + e < r) pe.x = 0.f;
+              if (qc + e + 1 < r) pe.y = 0.f;
+            }
+            const float2 dpd = __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                          make_float2(-dl.x, -dl.y));
+            const float2 dse = __fmul2_rn(pe, dpd);
+            pk[2 * e4 + h] = pack_bf16x2(pe.x, pe.y);
+            dk[2 * e4 + h] = pack_bf16x2(dse.x, dse.y);
           }
-          pk[2 * e4] = pack_bf16x2(pe[0], pe[1]);
-          pk[2 * e4 + 1] = pack_bf16x2(pe[2], pe[3]);
-          dk[2 * e4] = pack_bf16x2(dse[0], dse[1]);
-          dk[2 * e4 + 1] = pack_bf16x2(dse[2], dse[3]);
         }
         // P^T of query groups qc/16 and qc/16 + 1 over the first 8 of their own columns
         tmem_st8(tS + qc, pk);
