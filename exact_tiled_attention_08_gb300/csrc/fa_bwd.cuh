@@ -118,12 +118,16 @@ __global__ void __launch_bounds__(256)
 // them, or i >= j when causal) stream Q_i (with its rows' LSE log2(e) and
 // delta) and dO_i through a ring.  Per query block, in the transposed
 // orientation (TMEM lane = key, column = query):
-//   S^T = K_j Q_i^T and dP^T = V_j dO_i^T        (issuer A)
-//   P^T  = 2^(S^T scale log2e - LSE_i log2e), masked on the causal diagonal,
-//   dS^T = P^T o (dP^T - delta_i)                  (elementwise warps, thread = key)
-//   dK += dS^T Q_i, dQ_i = dS K_j, dV += P^T dO_i  (issuer B)
+//   S^T = K_j Q_i^T, then dP^T = V_j dO_i^T      (issuer A)
+//   P^T  = 2^(S^T scale log2e - LSE_i log2e), masked on the causal diagonal
+//                                                  (elementwise warps, thread = key)
+//   dV += P^T dO_i                                 (issuer B, as soon as P^T is written)
+//   dS^T = P^T o (dP^T - delta_i)                  (elementwise warps)
+//   dK += dS^T Q_i, dQ_i = dS K_j                  (issuer B)
 // and the reducer warps add dQ_i into the fp32 accumulator in global memory
-// while the next query block is processed.  dK, dV accumulate in TMEM across
+// while the next query block is processed.  The elementwise step is split in
+// two so that dV runs while dS^T is computed, and the next block's S^T (whose
+// columns dV frees) while dK and dQ run.  dK, dV accumulate in TMEM across
 // all query blocks and are written once at the end.
 //
 // The global fp32 reduction of dQ_i (64 KB per query block at d = 128) is
@@ -143,7 +147,7 @@ __global__ void __launch_bounds__(256)
 //               red.global.add.v4.f32, four whole lines per instruction
 //   warp  12    issuer A (S^T and dP^T) and TMEM owner
 //   warp  13    TMA producer
-//   warp  14    issuer B (dK, dQ, dV)
+//   warp  14    issuer B (dV, dK, dQ)
 //   warp  15    idle
 // Tensor memory: dK at column 0, dV at d, S^T at 2d, dP^T at 2d + 128.  The
 // bf16 P^T of query group G (queries 16G..16G+15) is written over the first 8
@@ -164,10 +168,14 @@ struct BwdCfg {
   static constexpr int kAtoms = D / 64;
   static constexpr int kSlots = (D == 128) ? 3 : 6;   // Q / dO ring
   static constexpr int kStatBytes = 1024;             // LSE*log2e and delta of one query block
-  // one entry per query block whose statistics can be in use or in flight:
-  // Q_i is loaded once the ring slot of fill 2i - kSlots is released, and by
-  // then the elementwise step of block i - (kSlots + 1) / 2 has finished
-  static constexpr int kStatEntries = (kSlots + 1) / 2;
+  // one entry per query block whose statistics can be in use or in flight.
+  // Q_i (and its statistics) is loaded once the slot of fill 2i - kSlots is
+  // released.  With an even kSlots that fill is Q_{i - kSlots/2}, released
+  // after dK, i.e. after the elementwise step of that block: kSlots/2 entries.
+  // With an odd kSlots it is dO_{i - (kSlots+1)/2}, released after dV, which
+  // may come before the second half of that block's elementwise step (which
+  // reads delta) has finished: one entry more.
+  static constexpr int kStatEntries = (kSlots % 2) ? (kSlots + 1) / 2 + 1 : kSlots / 2;
   static constexpr int kDsBytes = 128 * 128 * 2;      // dS^T tile: 2 atom columns of 64 queries
   static constexpr int kStageBytes = 4 * 4096;        // reducers' transposing tiles
   static constexpr int kThreads = 512;
@@ -184,7 +192,7 @@ struct BwdBarriers {
   uint64_t kv_full;
   uint64_t ring_full[8];
   uint64_t ring_empty[8];
-  uint64_t s_full, dp_full, ew_done, dv_done, dq_full, dq_free, acc_done;
+  uint64_t s_full, dp_full, p_done, ew_done, dv_done, dq_full, dq_free, acc_done;
   uint64_t drain[2];
   uint64_t never;  // signalled by nothing: the debug stall waits on it
   uint32_t tmem_base;
@@ -245,6 +253,7 @@ __global__ void __launch_bounds__(512, 1)
     }
     mbar_init(&bar->s_full, 1);
     mbar_init(&bar->dp_full, 1);
+    mbar_init(&bar->p_done, 256);
     mbar_init(&bar->ew_done, 256);
     mbar_init(&bar->dv_done, 1);
     mbar_init(&bar->dq_full, 1);
@@ -333,19 +342,15 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDpCol;
         bool ok = !(p.debug_stall && !wait_bounded_inl(&bar->never, 0, ctx, kSiteStall));
         ok = ok && wait_bounded_inl(&bar->kv_full, 0, ctx, kSiteBwdKV);
-        // With a three-slot ring dO_i comes in only after dK of the previous
-        // block has released Q_{i-1}'s slot, so S^T (whose Q_i was loaded long
-        // before) goes first; with more slots dP^T goes first, since the
-        // reducers free its columns before dV completes.
-        constexpr bool kSFirst = C::kSlots < 4;
+        // S^T goes first: the first half of the elementwise step needs only
+        // S^T, its columns are free as soon as dV of the previous block has
+        // run, and (with a three-slot ring) dO_i may still be on its way.
         for (int it = 0; ok && it < n_it; ++it) {
 #pragma unroll
           for (int step = 0; step < 2; ++step) {
-            if ((step == 0) == kSFirst) {
+            if (step == 0) {
               // S^T = K Q_i^T, once dV has consumed the previous P^T held in
-              // these columns (dv_done also covers the dK and dQ products
-              // issued before dV, so the dS^T tile of the previous block has
-              // been read as well)
+              // these columns
               const int fq = 2 * it, sq = fq % C::kSlots;
               if (!wait_bounded_inl(&bar->ring_full[sq], (fq / C::kSlots) & 1, ctx, kSiteBwdQ)) { ok = false; break; }
               if (it > 0 && !wait_bounded_inl(&bar->dv_done, (it - 1) & 1, ctx, kSiteBwdDvDone)) { ok = false; break; }
@@ -379,7 +384,7 @@ __global__ void __launch_bounds__(512, 1)
       }
       __syncwarp();
     } else if (warp == 14) {
-      // ---------------------------------------------------------------- issuer B: dK, dQ, dV
+      // ---------------------------------------------------------------- issuer B: dV, dK, dQ
       if (lane == 0) {
         constexpr uint32_t id_v = idesc_bf16_f32(128, D, false, true);  // dV (A = P^T in TMEM), dK
         constexpr uint32_t id_q = idesc_bf16_f32(128, D, true, true);   // dQ (A = dS, M-major)
@@ -392,9 +397,24 @@ __global__ void __launch_bounds__(512, 1)
         bool ok = true;
         for (int it = 0; ok && it < n_it; ++it) {
           const int sq = (2 * it) % C::kSlots, sd = (2 * it + 1) % C::kSlots;
+          // dV += P^T dO_i as soon as the elementwise warps have written P^T
+          // (P^T of query group kk sits at S^T column 16 kk) and dP^T, which
+          // also reads dO_i, is complete (so dO_i has landed, and its slot can
+          // be released after dV); this frees the S^T columns for the next
+          // block's scores
+          if (!wait_bounded_inl(&bar->dp_full, it & 1, ctx, kSiteBwdEw)) break;
+          if (!wait_bounded_inl(&bar->p_done, it & 1, ctx, kSiteBwdEw)) break;
+          tc_fence_after();
+          const uint64_t dodesc_mn = sdesc_sw128(ring + sd * C::kTileBytes, 16384, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ts(tDV, tS + kk * 16, dodesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
+                        (it > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bar->dv_done);
+          mma_commit(&bar->ring_empty[sd]);
+          // dK += dS^T Q_i once dS^T is written
           if (!wait_bounded_inl(&bar->ew_done, it & 1, ctx, kSiteBwdEw)) break;
           tc_fence_after();
-          // dK += dS^T Q_i
           const uint64_t qdesc_mn = sdesc_sw128(ring + sq * C::kTileBytes, 16384, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -403,7 +423,6 @@ __global__ void __launch_bounds__(512, 1)
                         (it > 0 || kk > 0) ? 1u : 0u);
           }
           // Q_i has been read by S^T (long complete) and dK: release its slot
-          // now, so that the next dO tile can come in while dQ and dV run
           mma_commit(&bar->ring_empty[sq]);
           // dQ_i = dS K (into the dP^T columns, all read by now)
 #pragma unroll
@@ -411,14 +430,6 @@ __global__ void __launch_bounds__(512, 1)
             mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4), id_q,
                         kk > 0 ? 1u : 0u);
           mma_commit(&bar->dq_full);
-          // dV += P^T dO_i: P^T of query group kk sits at S^T column 16 kk
-          const uint64_t dodesc_mn = sdesc_sw128(ring + sd * C::kTileBytes, 16384, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tDV, tS + kk * 16, dodesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
-                        (it > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bar->dv_done);
-          mma_commit(&bar->ring_empty[sd]);
         }
         mma_commit(&bar->acc_done);
         mma_commit(&bar->drain[1]);
@@ -483,53 +494,78 @@ __global__ void __launch_bounds__(512, 1)
     for (int it = 0; alive && it < n_it; ++it) {
       const int i = i_start + it;
       const float* stat = reinterpret_cast<const float*>(sStat + (it % C::kStatEntries) * C::kStatBytes);
-      // S^T of this block was issued after dV of the previous one, which also
-      // covers its dK and dQ: the dS^T tile is free to be overwritten
-      bool ok = wait_bounded_inl(&bar->s_full, it & 1, ctx, kSiteBwdS);
-      ok = ok && wait_bounded_inl(&bar->dp_full, it & 1, ctx, kSiteBwdDp);
-      if (!__all_sync(0xffffffffu, ok)) {
+      // ---- phase 1: P^T = 2^(S^T c - L log2e) into TMEM, the fp32 values kept
+      // in registers; issuer B starts dV as soon as all of P^T is written
+      if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->s_full, it & 1, ctx, kSiteBwdS))) {
         alive = false;
         break;
       }
       tc_fence_after();
       const bool diag = CAUSAL && (i == jb);
+      const float2 c2 = make_float2(sl2, sl2);
+      float2 pf[2][16];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int qc = 64 * g + 32 * ch;  // first query column of this chunk
-        uint32_t sv[32], dp[32];
+        uint32_t sv[32];
         tmem_ld32(tS + qc, sv);
-        tmem_ld32(tDP + qc, dp);
         tmem_wait_ld();
         reg_fence32(sv);
-        reg_fence32(dp);
-        uint32_t pk[16], dk[16];
-        const float2 c2 = make_float2(sl2, sl2);
+        uint32_t pk[16];
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          // four queries' L*log2e and delta (the same for every thread: broadcast reads)
+          // four queries' L*log2e (the same for every thread: a broadcast read)
           const float4 l4 = *reinterpret_cast<const float4*>(stat + qc + 4 * e4);
-          const float4 d4 = *reinterpret_cast<const float4*>(stat + 128 + qc + 4 * e4);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int e = 4 * e4 + 2 * h;  // two queries at a time (packed fp32x2 arithmetic)
             const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
-            const float2 dl = h ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
             const float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nl);
             float2 pe = make_float2(ex2_approx(xs.x), ex2_approx(xs.y));
             if (diag) {  // key k0 + r is in the future of query qbase + qc + e
               if (qc + e < r) pe.x = 0.f;
               if (qc + e + 1 < r) pe.y = 0.f;
             }
-            const float2 dpd = __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
-                                          make_float2(-dl.x, -dl.y));
-            const float2 dse = __fmul2_rn(pe, dpd);
+            pf[ch][e / 2] = pe;
             pk[2 * e4 + h] = pack_bf16x2(pe.x, pe.y);
-            dk[2 * e4 + h] = pack_bf16x2(dse.x, dse.y);
           }
         }
         // P^T of query groups qc/16 and qc/16 + 1 over the first 8 of their own columns
         tmem_st8(tS + qc, pk);
         tmem_st8(tS + qc + 16, pk + 8);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar->p_done);
+
+      // ---- phase 2: dS^T = P^T o (dP^T - delta) into the shared dS^T tile.
+      // dP^T of this block was issued after the reducers took the previous dQ
+      // out of TMEM, so the previous dK and dQ have finished reading the tile.
+      if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->dp_full, it & 1, ctx, kSiteBwdDp))) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int qc = 64 * g + 32 * ch;
+        uint32_t dp[32];
+        tmem_ld32(tDP + qc, dp);
+        tmem_wait_ld();
+        reg_fence32(dp);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(stat + 128 + qc + 4 * e4);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int e = 4 * e4 + 2 * h;
+            const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+            const float2 dpd = __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd);
+            const float2 dse = __fmul2_rn(pf[ch][e / 2], dpd);
+            dk[2 * e4 + h] = pack_bf16x2(dse.x, dse.y);
+          }
+        }
         // dS^T row r, queries [qc, qc+32): 4 chunks of 16 B in the swizzled atom g
 #pragma unroll
         for (int c16 = 0; c16 < 4; ++c16) {
@@ -538,7 +574,6 @@ __global__ void __launch_bounds__(512, 1)
               make_uint4(dk[4 * c16], dk[4 * c16 + 1], dk[4 * c16 + 2], dk[4 * c16 + 3]);
         }
       }
-      tmem_wait_st();
       fence_async_shared();
       tc_fence_before();
       mbar_arrive(&bar->ew_done);
