@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(256)
 //                                                  (elementwise warps, thread = key)
 //   dV += P^T dO_i                                 (issuer B, as soon as P^T is written)
 //   dS^T = P^T o (dP^T - delta_i)                  (elementwise warps)
-//   dK += dS^T Q_i, dQ_i = dS K_j                  (issuer B)
+//   dQ_i = dS K_j and dK += dS^T Q_i              (issuer B)
 // and the reducer warps add dQ_i into the fp32 accumulator in global memory
 // while the next query block is processed.  The elementwise step is split in
 // two so that dV runs while dS^T is computed, and the next block's S^T (whose
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(256)
 //               red.global.add.v4.f32, four whole lines per instruction
 //   warp  12    issuer A (S^T and dP^T) and TMEM owner
 //   warp  13    TMA producer
-//   warp  14    issuer B (dV, dK, dQ)
+//   warp  14    issuer B (dV, dQ and dK)
 //   warp  15    idle
 // Tensor memory: dK at column 0, dV at d, S^T at 2d, dP^T at 2d + 128.  The
 // bf16 P^T of query group G (queries 16G..16G+15) is written over the first 8
@@ -192,7 +192,7 @@ struct BwdBarriers {
   uint64_t kv_full;
   uint64_t ring_full[8];
   uint64_t ring_empty[8];
-  uint64_t s_full, dp_full, p_done, ew_done, dv_done, dq_full, dq_free, acc_done;
+  uint64_t s_full, dp_full, p_done, ew_done, dv_done, dq_full, dq_free, dk_done, acc_done;
   uint64_t drain[2];
   uint64_t never;  // signalled by nothing: the debug stall waits on it
   uint32_t tmem_base;
@@ -258,6 +258,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&bar->dv_done, 1);
     mbar_init(&bar->dq_full, 1);
     mbar_init(&bar->dq_free, 128);
+    mbar_init(&bar->dk_done, 1);
     mbar_init(&bar->acc_done, 1);
     mbar_init(&bar->drain[0], 1);
     mbar_init(&bar->drain[1], 1);
@@ -384,7 +385,7 @@ __global__ void __launch_bounds__(512, 1)
       }
       __syncwarp();
     } else if (warp == 14) {
-      // ---------------------------------------------------------------- issuer B: dV, dK, dQ
+      // ---------------------------------------------------------------- issuer B: dV, dQ and dK
       if (lane == 0) {
         constexpr uint32_t id_v = idesc_bf16_f32(128, D, false, true);  // dV (A = P^T in TMEM), dK
         constexpr uint32_t id_q = idesc_bf16_f32(128, D, true, true);   // dQ (A = dS, M-major)
@@ -412,24 +413,38 @@ __global__ void __launch_bounds__(512, 1)
                         (it > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bar->dv_done);
           mma_commit(&bar->ring_empty[sd]);
-          // dK += dS^T Q_i once dS^T is written
+          // dQ_i = dS K (into the dP^T columns, read by now) and dK += dS^T Q_i,
+          // once dS^T is written.  dQ goes first when the ring is deep enough
+          // to have the next dO tile already: the next dP^T waits for the
+          // reducers to take dQ out of these columns.  With a three-slot ring
+          // dK goes first, because the next dO tile can only be loaded once
+          // dK has released Q_i's slot.
           if (!wait_bounded_inl(&bar->ew_done, it & 1, ctx, kSiteBwdEw)) break;
           tc_fence_after();
           const uint64_t qdesc_mn = sdesc_sw128(ring + sq * C::kTileBytes, 16384, 1024);
+          constexpr bool kDqFirst = C::kSlots > 3;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-            mma_bf16_ss(tDK, dsdesc_k + off, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
-                        (it > 0 || kk > 0) ? 1u : 0u);
+          for (int step = 0; step < 2; ++step) {
+            if ((step == 0) == kDqFirst) {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4),
+                            id_q, kk > 0 ? 1u : 0u);
+              mma_commit(&bar->dq_full);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                mma_bf16_ss(tDK, dsdesc_k + off, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
+                            (it > 0 || kk > 0) ? 1u : 0u);
+              }
+              // Q_i has been read by S^T (long complete) and dK: release its
+              // slot; the dS^T tile is free for the next elementwise step once
+              // dQ has read it as well (dq_free, which the next dP^T waits for)
+              mma_commit(&bar->ring_empty[sq]);
+              mma_commit(&bar->dk_done);
+            }
           }
-          // Q_i has been read by S^T (long complete) and dK: release its slot
-          mma_commit(&bar->ring_empty[sq]);
-          // dQ_i = dS K (into the dP^T columns, all read by now)
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4), id_q,
-                        kk > 0 ? 1u : 0u);
-          mma_commit(&bar->dq_full);
         }
         mma_commit(&bar->acc_done);
         mma_commit(&bar->drain[1]);
@@ -538,10 +553,13 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_before();
       mbar_arrive(&bar->p_done);
 
-      // ---- phase 2: dS^T = P^T o (dP^T - delta) into the shared dS^T tile.
-      // dP^T of this block was issued after the reducers took the previous dQ
-      // out of TMEM, so the previous dK and dQ have finished reading the tile.
-      if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->dp_full, it & 1, ctx, kSiteBwdDp))) {
+      // ---- phase 2: dS^T = P^T o (dP^T - delta) into the shared dS^T tile,
+      // once the previous block's dK and dQ have read it (dP^T of this block
+      // was issued after the reducers took the previous dQ out of TMEM; dK,
+      // which runs after dQ, reports on its own)
+      bool ok2 = wait_bounded_inl(&bar->dp_full, it & 1, ctx, kSiteBwdDp);
+      if (it > 0) ok2 = ok2 && wait_bounded_inl(&bar->dk_done, (it - 1) & 1, ctx, kSiteBwdDp);
+      if (!__all_sync(0xffffffffu, ok2)) {
         alive = false;
         break;
       }
