@@ -56,12 +56,29 @@ struct FwdCfg {
   static constexpr int kTileRows = 128;
   static constexpr int kTileBytes = kTileRows * D * 2;  // Q, K, V tiles
   static constexpr int kAtoms = D / 64;                 // 64-column atom columns per tile
-  static constexpr int kSlots = (D == 128) ? 5 : 12;
   static constexpr int kThreads = 352;
   static constexpr uint32_t kTmemCols = 512;
+  // At d = 64 the tensor core also forms the row sums of the bf16 P that the
+  // output product uses: each V tile in the ring is followed by a tile of ones,
+  // the product O += P [V | 1] is 16 columns wider, and those columns hold
+  // sum_k P_rk, rescaled together with O.  At d = 128 the columns are not
+  // there (S 128 + P 2 x 64 + O 2 x 128 = 512) and the softmax sums them.
+  static constexpr bool kSumByMma = (D == 64);
+  static constexpr int kOCols = kSumByMma ? D + 16 : D;  // O accumulator columns
+  static constexpr int kOnesBytes = kSumByMma ? 16384 : 0;
+  // K_j is ring fill 2j, V_j fill 2j+1; with the ones tiles the slots come in
+  // pairs (K, V, ones), so the slot count is even
+  static constexpr int kSlots = (D == 128) ? 5 : 8;
+  static_assert(!kSumByMma || kSlots % 2 == 0, "K/V slot pairs");
+  static constexpr int kStageBytes = 2 * kTileBytes + kOnesBytes;
+  static constexpr int kRingBytes = kSumByMma ? (kSlots / 2) * kStageBytes : kSlots * kTileBytes;
+  static __device__ __host__ constexpr int slot_offset(int s) {
+    return kSumByMma ? (s / 2) * kStageBytes + (s & 1) * kTileBytes : s * kTileBytes;
+  }
   static constexpr uint32_t kSCol = 0, kPCol0 = 128, kPCol1 = 192;
-  static constexpr uint32_t kOCol0 = 256, kOCol1 = 256 + D;
-  static constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kSlots * kTileBytes + 512;
+  static constexpr uint32_t kOCol0 = 256, kOCol1 = 256 + kOCols;
+  static_assert(kOCol1 + kOCols <= kTmemCols, "tensor memory budget");
+  static constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kRingBytes + 512;
 };
 
 struct FwdBarriers {
@@ -101,7 +118,7 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sKV = smem + 2 * C::kTileBytes;
-  FwdBarriers* bar = reinterpret_cast<FwdBarriers*>(sKV + C::kSlots * C::kTileBytes);
+  FwdBarriers* bar = reinterpret_cast<FwdBarriers*>(sKV + C::kRingBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N;
@@ -117,6 +134,14 @@ __global__ void __launch_bounds__(352, 1)
   const int nb1 = has1 ? (CAUSAL ? min(nblk, 2 * pair + 2) : nblk) : 0;
   const int nb_max = max(nb0, nb1);
 
+  if (C::kSumByMma) {
+    // the ones tiles (bf16 1.0) after each V slot, read by the tensor core
+    for (int st = 0; st < C::kSlots / 2; ++st) {
+      uint4* ones = reinterpret_cast<uint4*>(sKV + st * C::kStageBytes + 2 * C::kTileBytes);
+      for (int i = tid; i < C::kOnesBytes / 16; i += C::kThreads) ones[i] = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+    }
+    fence_async_shared();
+  }
   if (tid == 0) {
     mbar_init(&bar->q_full, 1);
     for (int s = 0; s < C::kSlots; ++s) {
@@ -171,7 +196,7 @@ __global__ void __launch_bounds__(352, 1)
           mbar_arrive_expect_tx(&bar->kv_full[s], C::kTileBytes);
           const CUtensorMap* map = kv ? &map_v : &map_k;
           for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_3d(sKV + s * C::kTileBytes + a * 16384, map, &bar->kv_full[s], a * 64, j * 128, bh);
+            tma_load_3d(sKV + C::slot_offset(s) + a * 16384, map, &bar->kv_full[s], a * 64, j * 128, bh);
           ++fill;
         }
       }
@@ -200,7 +225,7 @@ __global__ void __launch_bounds__(352, 1)
         const int f = 2 * j;
         const int ks = f % C::kSlots;
         if (!wait_bounded(&bar->kv_full[ks], (f / C::kSlots) & 1, ctx, kSiteFwdK)) break;
-        const uint64_t kdesc = sdesc_sw128(skv + ks * C::kTileBytes, 16, 1024);
+        const uint64_t kdesc = sdesc_sw128(skv + C::slot_offset(ks), 16, 1024);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (j < (t ? nb1 : nb0)) {
@@ -232,13 +257,14 @@ __global__ void __launch_bounds__(352, 1)
     // V_j is ring fill 2j+1; O_t += P_t(j) V_j once the softmax of tile t wrote P_t(j)
     if (lane == 0) {
       const uint32_t skv = smem_u32(sKV);
-      constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t id_pv = idesc_bf16_f32(128, C::kOCols, false, true);
       bool ok = true;
       for (int j = 0; ok && j < nb_max; ++j) {
         const int f = 2 * j + 1;
         const int vs = f % C::kSlots;
         if (!wait_bounded(&bar->kv_full[vs], (f / C::kSlots) & 1, ctx, kSiteFwdV)) break;
-        const uint64_t vdesc = sdesc_sw128(skv + vs * C::kTileBytes, 16384, 1024);
+        // (with the row sums, the second 64-column block of B is the ones tile)
+        const uint64_t vdesc = sdesc_sw128(skv + C::slot_offset(vs), 16384, 1024);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (j < (t ? nb1 : nb0)) {
@@ -346,6 +372,7 @@ __global__ void __launch_bounds__(352, 1)
       float2 acc[4], acc_mma[4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) acc[a] = acc_mma[a] = make_float2(0.f, 0.f);
+      // (at d = 64 the sums of the rounded values come from the tensor core)
       uint32_t pk[4][16];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -357,14 +384,15 @@ __global__ void __launch_bounds__(352, 1)
           const float p1 = ex2_approx(x.y);
           pk[c][i] = pack_bf16x2(p0, p1);
           acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
-          acc_mma[i & 3] = __fadd2_rn(acc_mma[i & 3], make_float2(__uint_as_float(pk[c][i] << 16),
-                                                                 __uint_as_float(pk[c][i] & 0xffff0000u)));
+          if (!C::kSumByMma)
+            acc_mma[i & 3] = __fadd2_rn(acc_mma[i & 3], make_float2(__uint_as_float(pk[c][i] << 16),
+                                                                   __uint_as_float(pk[c][i] & 0xffff0000u)));
         }
       }
       const float2 accs = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
       const float2 accm = __fadd2_rn(__fadd2_rn(acc_mma[0], acc_mma[1]), __fadd2_rn(acc_mma[2], acc_mma[3]));
       l = l * alpha + (accs.x + accs.y);
-      l_mma = l_mma * alpha + (accm.x + accm.y);
+      if (!C::kSumByMma) l_mma = l_mma * alpha + (accm.x + accm.y);
       // P_t and O_t are in use until O_t += P_t(j-1) V_{j-1} has completed
       if (j > 0) {
         if (!__all_sync(0xffffffffu, wait_bounded(&bar->pv_done[t], (j - 1) & 1, ctx, kSiteFwdPvDone))) {
@@ -385,6 +413,16 @@ __global__ void __launch_bounds__(352, 1)
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
           tmem_st32(tO + 32 * c, ov);
         }
+        if (C::kSumByMma) {
+          // the row sums of the rounded P are rescaled with O
+          uint32_t sv[16];
+          tmem_ld16(tO + D, sv);
+          tmem_wait_ld();
+          reg_fence16(sv);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sv[i] = __float_as_uint(__uint_as_float(sv[i]) * alpha);
+          tmem_st16(tO + D, sv);
+        }
         tmem_wait_st();
       }
 #pragma unroll
@@ -393,10 +431,17 @@ __global__ void __launch_bounds__(352, 1)
       tc_fence_before();
       mbar_arrive(&bar->p_full[t]);
     }
-    // epilogue: O = o / l_mma, LSE = (m + log2 l) ln 2
+    // epilogue: O = o / l_mma (at d = 64 from the extra O columns), LSE = (m + log2 l) ln 2
     if (alive) {
       if (__all_sync(0xffffffffu, wait_bounded(&bar->pv_done[t], (nb - 1) & 1, ctx, kSiteFwdO))) {
         tc_fence_after();
+        if (C::kSumByMma) {
+          uint32_t sv[16];
+          tmem_ld16(tO + D, sv);
+          tmem_wait_ld();
+          reg_fence16(sv);
+          l_mma = __uint_as_float(sv[0]);
+        }
         const float inv_l = 1.f / l_mma;
         __nv_bfloat16* orow = p.o + ((size_t)bh * N + row_g) * D;
 #pragma unroll
