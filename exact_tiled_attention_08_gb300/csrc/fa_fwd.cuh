@@ -9,8 +9,12 @@
 // "Why did Blackwell need FlashAttention-4?": accumulators in tensor memory,
 // conditional rescaling.
 //
-// One CTA owns two query tiles of 128 rows (a "tile pair") of one (batch,
-// head).  Warp roles (352 threads):
+// The work item is a pair of 128-row query tiles (a "tile pair") of one
+// (batch, head).  The kernel is persistent: one CTA per SM walks a fixed
+// sequence of items (fwd_item below), and the roles run on from one item to
+// the next without draining, so the next pair's queries load while the
+// tensor core finishes the current pair and its epilogue overlaps the next
+// pair's first score products.  Warp roles (352 threads):
 //   warps 0-3  softmax warpgroup of tile 0 (thread = query row)
 //   warps 4-7  softmax warpgroup of tile 1
 //   warp  8    issues the score products S = Q K^T (one thread); TMEM owner
@@ -83,6 +87,7 @@ struct FwdCfg {
 
 struct FwdBarriers {
   uint64_t q_full;
+  uint64_t q_empty;     // the S products of the CTA's current tile pair are complete (MMA commit)
   uint64_t kv_full[16];
   uint64_t kv_empty[16];
   uint64_t s_full[2];   // S holds tile t's scores (MMA commit)
@@ -99,7 +104,10 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int N;
-  int num_pairs;
+  int num_pairs;   // tile pairs per (batch, head)
+  int num_bh;      // B * H
+  int pair_items;  // pairs (by rank) processed as pairs; the rest as single tiles
+  int num_items;   // pair_items + 2 (num_pairs num_bh - pair_items)
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
   int debug_stall;  // nonzero: the MMA thread first waits on `never` (tests the timeout path)
@@ -107,7 +115,57 @@ struct FwdParams {
 
 // wait sites reported in the status word
 enum : int { kSiteStall = 0, kSiteFwdProducer = 1, kSiteFwdQ, kSiteFwdK, kSiteFwdV, kSiteFwdSFree, kSiteFwdP,
-             kSiteFwdS, kSiteFwdO, kSiteFwdPvDone };
+             kSiteFwdS, kSiteFwdO, kSiteFwdPvDone, kSiteFwdQEmpty };
+
+// One work item: a pair of 128-row query tiles of one (batch, head), or a
+// single tile (nb1 = 0).
+struct FwdItem {
+  int bh;
+  int q0;        // first query row of tile 0
+  int nb0, nb1;  // key blocks visited by tile 0 and tile 1 (0: no such tile)
+};
+
+// The CTAs are persistent: CTA c takes, in round k, the item of rank
+// k G + c (even k) or k G + G - 1 - c (odd k), G = gridDim.x.  Pairs are
+// ranked so that consecutive ranks cost about the same: with the causal mask
+// the cost of a pair grows with its position, and the ranks run over the
+// pairs from the last (heaviest) to the first, each pair across all heads;
+// the alternating direction then evens out the CTAs' totals.  Without the
+// mask every pair costs the same and the ranks run head by head, so that
+// the CTAs working at the same time share each head's keys and values in L2.
+// The pairs of rank >= pair_items are split into their two tiles, each an
+// item of its own (ranks pair_items + 2 (rank - pair_items) + tile), so that
+// a last round with fewer pairs than CTAs takes about the time of one tile.
+template <bool CAUSAL>
+__device__ __forceinline__ bool fwd_item(const FwdParams& p, int k, FwdItem& w) {
+  // (ranks fit in int: there are fewer than 2^31 / 2^14 items, see fa_fwd's limits)
+  const int G = gridDim.x;
+  const int c = blockIdx.x;
+  const int r = k * G + ((k & 1) ? G - 1 - c : c);
+  if (r >= p.num_items) return false;
+  const bool single = r >= p.pair_items;
+  const int pr = single ? p.pair_items + ((r - p.pair_items) >> 1) : r;  // pair rank
+  int pair;
+  if (CAUSAL) {
+    pair = p.num_pairs - 1 - pr / p.num_bh;
+    w.bh = pr % p.num_bh;
+  } else {
+    pair = pr % p.num_pairs;
+    w.bh = pr / p.num_pairs;
+  }
+  const int nblk = (p.N + 127) / 128;
+  if (single) {
+    const int tile = (r - p.pair_items) & 1;
+    w.q0 = pair * 256 + 128 * tile;
+    w.nb0 = w.q0 < p.N ? (CAUSAL ? min(nblk, 2 * pair + 1 + tile) : nblk) : 0;  // 0: past N, nothing to do
+    w.nb1 = 0;
+  } else {
+    w.q0 = pair * 256;
+    w.nb0 = CAUSAL ? min(nblk, 2 * pair + 1) : nblk;
+    w.nb1 = w.q0 + 128 < p.N ? (CAUSAL ? min(nblk, 2 * pair + 2) : nblk) : 0;
+  }
+  return true;
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(352, 1)
@@ -123,17 +181,6 @@ __global__ void __launch_bounds__(352, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N;
 
-  // work item: pairs of a head are visited from the last (heaviest when causal) to the first
-  const int pr = blockIdx.x % p.num_pairs;
-  const int bh = blockIdx.x / p.num_pairs;
-  const int pair = p.num_pairs - 1 - pr;
-  const int q0 = pair * 256;
-  const bool has1 = q0 + 128 < N;
-  const int nblk = (N + 127) / 128;
-  const int nb0 = CAUSAL ? min(nblk, 2 * pair + 1) : nblk;
-  const int nb1 = has1 ? (CAUSAL ? min(nblk, 2 * pair + 2) : nblk) : 0;
-  const int nb_max = max(nb0, nb1);
-
   if (C::kSumByMma) {
     // the ones tiles (bf16 1.0) after each V slot, read by the tensor core
     for (int st = 0; st < C::kSlots / 2; ++st) {
@@ -144,6 +191,7 @@ __global__ void __launch_bounds__(352, 1)
   }
   if (tid == 0) {
     mbar_init(&bar->q_full, 1);
+    mbar_init(&bar->q_empty, 1);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(&bar->kv_full[s], 1);
       mbar_init(&bar->kv_empty[s], 1);
@@ -175,33 +223,51 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t tmem = bar->tmem_base;
   const WaitCtx ctx{&bar->abort_flag, p.wait_limit_ns};
 
+  // Every role walks the same sequence of items; the ring fills, the uses of
+  // S and the per-tile products are counted across items, so barrier phases
+  // carry over from one item to the next.
   if (warp == 9) {
     // ------------------------------------------------------------------ TMA producer
-    // fill order = consumption order: K_0, V_0, K_1, V_1, ...
+    // fill order = consumption order: K_0, V_0, K_1, V_1, ... of each item in turn
     if (lane == 0) {
-      int fill = 0;
-      mbar_arrive_expect_tx(&bar->q_full, C::kTileBytes * (has1 ? 2 : 1));
-      for (int t = 0; t < (has1 ? 2 : 1); ++t)
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &map_q, &bar->q_full, a * 64, q0 + 128 * t, bh);
+      int fill = 0, nq = 0;
       bool ok = true;
-      for (int j = 0; ok && j < nb_max; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int s = fill % C::kSlots;
-          const uint32_t u = fill / C::kSlots;
-          if (!wait_bounded(&bar->kv_empty[s], (u & 1) ^ 1, ctx, kSiteFwdProducer)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&bar->kv_full[s], C::kTileBytes);
-          const CUtensorMap* map = kv ? &map_v : &map_k;
+      auto load_kv = [&](int j, int kv, int bh) -> bool {
+        const int s = fill % C::kSlots;
+        const uint32_t u = fill / C::kSlots;
+        if (!wait_bounded(&bar->kv_empty[s], (u & 1) ^ 1, ctx, kSiteFwdProducer)) return false;
+        mbar_arrive_expect_tx(&bar->kv_full[s], C::kTileBytes);
+        const CUtensorMap* map = kv ? &map_v : &map_k;
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_3d(sKV + C::slot_offset(s) + a * 16384, map, &bar->kv_full[s], a * 64, j * 128, bh);
+        ++fill;
+        return true;
+      };
+      FwdItem w;
+      for (int k = 0; ok && fwd_item<CAUSAL>(p, k, w); ++k) {
+        const int nb_max = max(w.nb0, w.nb1);
+        if (nb_max == 0) continue;  // a single tile past N
+        const bool has1 = w.nb1 > 0;
+        // the first key/value block needs only ring slots: it goes out
+        // before Q, whose buffer the previous item may still be reading
+        ok = load_kv(0, 0, w.bh) && load_kv(0, 1, w.bh);
+        if (ok && nq > 0) ok = wait_bounded(&bar->q_empty, (nq - 1) & 1, ctx, kSiteFwdQEmpty);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bar->q_full, C::kTileBytes * (has1 ? 2 : 1));
+        for (int t = 0; t < (has1 ? 2 : 1); ++t)
           for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_3d(sKV + C::slot_offset(s) + a * 16384, map, &bar->kv_full[s], a * 64, j * 128, bh);
-          ++fill;
-        }
+            tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &map_q, &bar->q_full, a * 64, w.q0 + 128 * t, w.bh);
+        ++nq;
+        // the next item's queries go to L2 now, so that their load at the
+        // item boundary is served from there
+        FwdItem nx;
+        if (fwd_item<CAUSAL>(p, k + 1, nx) && nx.nb0 > 0)
+          for (int t = 0; t < (nx.nb1 > 0 ? 2 : 1); ++t)
+            for (int a = 0; a < C::kAtoms; ++a) tma_prefetch_l2_3d(&map_q, a * 64, nx.q0 + 128 * t, nx.bh);
+        for (int j = 1; ok && j < nb_max; ++j) ok = load_kv(j, 0, w.bh) && load_kv(j, 1, w.bh);
       }
       // every copy this thread started must land before the CTA can exit
-      wait_drain(&bar->q_full, 0, kDrainLimitNs);
+      if (nq > 0) wait_drain(&bar->q_full, (nq - 1) & 1, kDrainLimitNs);
       for (int s = 0; s < C::kSlots; ++s) {
         if (fill > s) {
           const int uses = (fill - 1 - s) / C::kSlots + 1;
@@ -212,40 +278,53 @@ __global__ void __launch_bounds__(352, 1)
     __syncwarp();
   } else if (warp == 8) {
     // ------------------------------------------------------------------ S issuer
-    // K_j is ring fill 2j; S(k) waits until the tile that used S before has loaded it
+    // K_j is ring fill 2g (g counts key blocks over all items); S(k) waits
+    // until the tile that used S before has loaded it
     if (lane == 0) {
       const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
       const uint64_t qdesc0 = sdesc_sw128(sq, 16, 1024);
       const uint64_t qdesc1 = sdesc_sw128(sq + C::kTileBytes, 16, 1024);
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-      int s_uses = 0;
+      int s_uses = 0, g = 0, nq = 0;
       bool ok = !(p.debug_stall && !wait_bounded(&bar->never, 0, ctx, kSiteStall));
-      ok = ok && wait_bounded(&bar->q_full, 0, ctx, kSiteFwdQ);
-      for (int j = 0; ok && j < nb_max; ++j) {
-        const int f = 2 * j;
-        const int ks = f % C::kSlots;
-        if (!wait_bounded(&bar->kv_full[ks], (f / C::kSlots) & 1, ctx, kSiteFwdK)) break;
-        const uint64_t kdesc = sdesc_sw128(skv + C::slot_offset(ks), 16, 1024);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (j < (t ? nb1 : nb0)) {
-            if (s_uses > 0 && !wait_bounded(&bar->s_free, (s_uses - 1) & 1, ctx, kSiteFwdSFree)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t qd = t ? qdesc1 : qdesc0;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-              mma_bf16_ss(tmem + C::kSCol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&bar->s_full[t]);
-            ++s_uses;
+      FwdItem w;
+      for (int k = 0; ok && fwd_item<CAUSAL>(p, k, w); ++k) {
+        const int nb_max = max(w.nb0, w.nb1);
+        if (nb_max == 0) continue;
+        if (!wait_bounded(&bar->q_full, nq & 1, ctx, kSiteFwdQ)) break;
+        ++nq;
+        for (int j = 0; ok && j < nb_max; ++j, ++g) {
+          const int f = 2 * g;
+          const int ks = f % C::kSlots;
+          if (!wait_bounded(&bar->kv_full[ks], (f / C::kSlots) & 1, ctx, kSiteFwdK)) {
+            ok = false;
+            break;
           }
+          const uint64_t kdesc = sdesc_sw128(skv + C::slot_offset(ks), 16, 1024);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (j < (t ? w.nb1 : w.nb0)) {
+              if (s_uses > 0 && !wait_bounded(&bar->s_free, (s_uses - 1) & 1, ctx, kSiteFwdSFree)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t qd = t ? qdesc1 : qdesc0;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                mma_bf16_ss(tmem + C::kSCol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&bar->s_full[t]);
+              ++s_uses;
+            }
+          }
+          if (!ok) break;
+          mma_commit(&bar->kv_empty[ks]);
         }
         if (!ok) break;
-        mma_commit(&bar->kv_empty[ks]);
+        // the item's queries have been read: their buffer may take the next item's
+        mma_commit(&bar->q_empty);
       }
       // everything issued must complete before the tensor memory is released
       mma_commit(&bar->drain[0]);
@@ -254,36 +333,47 @@ __global__ void __launch_bounds__(352, 1)
     __syncwarp();
   } else if (warp == 10) {
     // ------------------------------------------------------------------ P V issuer
-    // V_j is ring fill 2j+1; O_t += P_t(j) V_j once the softmax of tile t wrote P_t(j)
+    // V_j is ring fill 2g+1; O_t += P_t(j) V_j once the softmax of tile t wrote P_t(j)
     if (lane == 0) {
       const uint32_t skv = smem_u32(sKV);
       constexpr uint32_t id_pv = idesc_bf16_f32(128, C::kOCols, false, true);
+      int g = 0;
+      int pv_uses[2] = {0, 0};
       bool ok = true;
-      for (int j = 0; ok && j < nb_max; ++j) {
-        const int f = 2 * j + 1;
-        const int vs = f % C::kSlots;
-        if (!wait_bounded(&bar->kv_full[vs], (f / C::kSlots) & 1, ctx, kSiteFwdV)) break;
-        // (with the row sums, the second 64-column block of B is the ones tile)
-        const uint64_t vdesc = sdesc_sw128(skv + C::slot_offset(vs), 16384, 1024);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (j < (t ? nb1 : nb0)) {
-            if (!wait_bounded(&bar->p_full[t], j & 1, ctx, kSiteFwdP)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t dcol = tmem + (t ? C::kOCol1 : C::kOCol0);
-            const uint32_t pcol = tmem + (t ? C::kPCol1 : C::kPCol0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_bf16_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 2048) >> 4), id_pv,
-                          (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&bar->pv_done[t]);
+      FwdItem w;
+      for (int k = 0; ok && fwd_item<CAUSAL>(p, k, w); ++k) {
+        const int nb_max = max(w.nb0, w.nb1);
+        if (nb_max == 0) continue;
+        for (int j = 0; ok && j < nb_max; ++j, ++g) {
+          const int f = 2 * g + 1;
+          const int vs = f % C::kSlots;
+          if (!wait_bounded(&bar->kv_full[vs], (f / C::kSlots) & 1, ctx, kSiteFwdV)) {
+            ok = false;
+            break;
           }
+          // (with the row sums, the second 64-column block of B is the ones tile)
+          const uint64_t vdesc = sdesc_sw128(skv + C::slot_offset(vs), 16384, 1024);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (j < (t ? w.nb1 : w.nb0)) {
+              if (!wait_bounded(&bar->p_full[t], pv_uses[t] & 1, ctx, kSiteFwdP)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t dcol = tmem + (t ? C::kOCol1 : C::kOCol0);
+              const uint32_t pcol = tmem + (t ? C::kPCol1 : C::kPCol0);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 2048) >> 4), id_pv,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(&bar->pv_done[t]);
+              ++pv_uses[t];
+            }
+          }
+          if (!ok) break;
+          mma_commit(&bar->kv_empty[vs]);
         }
-        if (!ok) break;
-        mma_commit(&bar->kv_empty[vs]);
       }
       mma_commit(&bar->drain[1]);
       wait_drain(&bar->drain[1], 0, kDrainLimitNs);
@@ -294,177 +384,191 @@ __global__ void __launch_bounds__(352, 1)
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
-    const int nb = t ? nb1 : nb0;
-    const int row_g = q0 + 128 * t + r;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + C::kSCol + lane_off;
     const uint32_t tP = tmem + (t ? C::kPCol1 : C::kPCol0) + lane_off;
     const uint32_t tO = tmem + (t ? C::kOCol1 : C::kOCol0) + lane_off;
     const float sl2 = p.scale_log2;
-    float m = -CUDART_INF_F;  // exponent reference (log2 units), a stale running max
-    float l = 0.f, l_mma = 0.f;
-    bool alive = nb > 0;
-    for (int j = 0; alive && j < nb; ++j) {
-      if (!__all_sync(0xffffffffu, wait_bounded(&bar->s_full[t], j & 1, ctx, kSiteFwdS))) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
-      // the scores are in registers: the other tile's scores may now overwrite S
-      tc_fence_before();
-      mbar_arrive(&bar->s_free);
-
-      const int kbase = j * 128;
-      const bool tail = kbase + 128 > N;
-      const bool diag = CAUSAL && (kbase + 127 > q0 + 128 * t);
-      if (tail || diag) {
-        const int last = (CAUSAL ? min(N - 1, row_g) : N - 1) - kbase;  // last visible key of this row
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > last) sr[c >> 5][c & 31] = __float_as_uint(-CUDART_INF_F);
-      }
-      // row maximum as a tree of 3-input maxima
-      float mx;
-      {
-        float t1[43];
-#pragma unroll
-        for (int i = 0; i < 42; ++i)
-          t1[i] = max3(__uint_as_float(sr[(3 * i) >> 5][(3 * i) & 31]),
-                       __uint_as_float(sr[(3 * i + 1) >> 5][(3 * i + 1) & 31]),
-                       __uint_as_float(sr[(3 * i + 2) >> 5][(3 * i + 2) & 31]));
-        t1[42] = fmaxf(__uint_as_float(sr[3][30]), __uint_as_float(sr[3][31]));
-        float t2[15];
-#pragma unroll
-        for (int i = 0; i < 14; ++i) t2[i] = max3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
-        t2[14] = t1[42];
-        float t3[5];
-#pragma unroll
-        for (int i = 0; i < 5; ++i) t3[i] = max3(t2[3 * i], t2[3 * i + 1], t2[3 * i + 2]);
-        mx = max3(max3(t3[0], t3[1], t3[2]), t3[3], t3[4]);
-      }
-      const float m_new = fmaxf(m, mx * sl2);
-      // conditional rescale: move the exponent reference only when the row
-      // maximum rose by more than the threshold (always on the first block)
-      float alpha = 1.f;
-      bool rescale_warp = false;
-      if (j == 0) {
-        m = m_new;
-      } else {
-        const bool need = (m_new - m) > kRescaleThresholdLog2;
-        rescale_warp = __any_sync(0xffffffffu, need);
-        if (need) {
-          alpha = ex2_approx(m - m_new);
-          m = m_new;
-        }
-      }
-      // p = 2^(s c - m) two at a time.  Two row sums are kept: `l` of the fp32
-      // probabilities (for the LSE) and `l_mma` of the bf16-rounded ones that
-      // the P V product uses (for the normalisation of O, so that the rounding
-      // of a dominant probability cancels); four partial sums each.
-      const float2 c2 = make_float2(sl2, sl2);
-      const float2 mneg2 = make_float2(-m, -m);
-      float2 acc[4], acc_mma[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) acc[a] = acc_mma[a] = make_float2(0.f, 0.f);
-      // (at d = 64 the sums of the rounded values come from the tensor core)
-      uint32_t pk[4][16];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
-                                      c2, mneg2);
-          const float p0 = ex2_approx(x.x);
-          const float p1 = ex2_approx(x.y);
-          pk[c][i] = pack_bf16x2(p0, p1);
-          acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
-          if (!C::kSumByMma)
-            acc_mma[i & 3] = __fadd2_rn(acc_mma[i & 3], make_float2(__uint_as_float(pk[c][i] << 16),
-                                                                   __uint_as_float(pk[c][i] & 0xffff0000u)));
-        }
-      }
-      const float2 accs = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-      const float2 accm = __fadd2_rn(__fadd2_rn(acc_mma[0], acc_mma[1]), __fadd2_rn(acc_mma[2], acc_mma[3]));
-      l = l * alpha + (accs.x + accs.y);
-      if (!C::kSumByMma) l_mma = l_mma * alpha + (accm.x + accm.y);
-      // P_t and O_t are in use until O_t += P_t(j-1) V_{j-1} has completed
-      if (j > 0) {
-        if (!__all_sync(0xffffffffu, wait_bounded(&bar->pv_done[t], (j - 1) & 1, ctx, kSiteFwdPvDone))) {
+    int uses = 0;  // blocks this tile has processed over all items (= S loads = P V products)
+    bool alive = true;
+    FwdItem w;
+    for (int k = 0; alive && fwd_item<CAUSAL>(p, k, w); ++k) {
+      const int nb = t ? w.nb1 : w.nb0;
+      if (nb == 0) continue;
+      const int row_q0 = w.q0 + 128 * t;  // first query row of this tile
+      const int row_g = row_q0 + r;
+      float m = -CUDART_INF_F;  // exponent reference (log2 units), a stale running max
+      float l = 0.f, l_mma = 0.f;
+      for (int j = 0; j < nb; ++j, ++uses) {
+        if (!__all_sync(0xffffffffu, wait_bounded(&bar->s_full[t], uses & 1, ctx, kSiteFwdS))) {
           alive = false;
           break;
         }
         tc_fence_after();
-      }
-      if (rescale_warp) {
-        // correction O <- alpha O, in place in tensor memory
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(tO + 32 * c, ov);
-          tmem_wait_ld();
-          reg_fence32(ov);
+        uint32_t sr[4][32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32(tO + 32 * c, ov);
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
+        // the scores are in registers: the other tile's scores may now overwrite S
+        tc_fence_before();
+        mbar_arrive(&bar->s_free);
+
+        const int kbase = j * 128;
+        const bool tail = kbase + 128 > N;
+        const bool diag = CAUSAL && (kbase + 127 > row_q0);
+        if (tail || diag) {
+          const int last = (CAUSAL ? min(N - 1, row_g) : N - 1) - kbase;  // last visible key of this row
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > last) sr[c >> 5][c & 31] = __float_as_uint(-CUDART_INF_F);
         }
-        if (C::kSumByMma) {
-          // the row sums of the rounded P are rescaled with O
-          uint32_t sv[16];
-          tmem_ld16(tO + D, sv);
-          tmem_wait_ld();
-          reg_fence16(sv);
+        // row maximum as a tree of 3-input maxima
+        float mx;
+        {
+          float t1[43];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) sv[i] = __float_as_uint(__uint_as_float(sv[i]) * alpha);
-          tmem_st16(tO + D, sv);
+          for (int i = 0; i < 42; ++i)
+            t1[i] = max3(__uint_as_float(sr[(3 * i) >> 5][(3 * i) & 31]),
+                         __uint_as_float(sr[(3 * i + 1) >> 5][(3 * i + 1) & 31]),
+                         __uint_as_float(sr[(3 * i + 2) >> 5][(3 * i + 2) & 31]));
+          t1[42] = fmaxf(__uint_as_float(sr[3][30]), __uint_as_float(sr[3][31]));
+          float t2[15];
+#pragma unroll
+          for (int i = 0; i < 14; ++i) t2[i] = max3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
+          t2[14] = t1[42];
+          float t3[5];
+#pragma unroll
+          for (int i = 0; i < 5; ++i) t3[i] = max3(t2[3 * i], t2[3 * i + 1], t2[3 * i + 2]);
+          mx = max3(max3(t3[0], t3[1], t3[2]), t3[3], t3[4]);
         }
-        tmem_wait_st();
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_st16(tP + 16 * c, pk[c]);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bar->p_full[t]);
-    }
-    // epilogue: O = o / l_mma (at d = 64 from the extra O columns), LSE = (m + log2 l) ln 2
-    if (alive) {
-      if (__all_sync(0xffffffffu, wait_bounded(&bar->pv_done[t], (nb - 1) & 1, ctx, kSiteFwdO))) {
-        tc_fence_after();
-        if (C::kSumByMma) {
-          uint32_t sv[16];
-          tmem_ld16(tO + D, sv);
-          tmem_wait_ld();
-          reg_fence16(sv);
-          l_mma = __uint_as_float(sv[0]);
-        }
-        const float inv_l = 1.f / l_mma;
-        __nv_bfloat16* orow = p.o + ((size_t)bh * N + row_g) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(tO + 32 * c, ov);
-          tmem_wait_ld();
-          reg_fence32(ov);
-          if (row_g < N) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(ov[8 * v4 + 0]) * inv_l, __uint_as_float(ov[8 * v4 + 1]) * inv_l);
-              w.y = pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * inv_l, __uint_as_float(ov[8 * v4 + 3]) * inv_l);
-              w.z = pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * inv_l, __uint_as_float(ov[8 * v4 + 5]) * inv_l);
-              w.w = pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * inv_l, __uint_as_float(ov[8 * v4 + 7]) * inv_l);
-              dst[v4] = w;
-            }
+        const float m_new = fmaxf(m, mx * sl2);
+        // conditional rescale: move the exponent reference only when the row
+        // maximum rose by more than the threshold (always on the first block)
+        float alpha = 1.f;
+        bool rescale_warp = false;
+        if (j == 0) {
+          m = m_new;
+        } else {
+          const bool need = (m_new - m) > kRescaleThresholdLog2;
+          rescale_warp = __any_sync(0xffffffffu, need);
+          if (need) {
+            alpha = ex2_approx(m - m_new);
+            m = m_new;
           }
         }
-        if (row_g < N) p.lse[(size_t)bh * N + row_g] = (m + log2f(l)) * 0.6931471805599453f;
+        // p = 2^(s c - m) two at a time.  Two row sums are kept: `l` of the fp32
+        // probabilities (for the LSE) and `l_mma` of the bf16-rounded ones that
+        // the P V product uses (for the normalisation of O, so that the rounding
+        // of a dominant probability cancels); four partial sums each.
+        const float2 c2 = make_float2(sl2, sl2);
+        const float2 mneg2 = make_float2(-m, -m);
+        float2 acc[4], acc_mma[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) acc[a] = acc_mma[a] = make_float2(0.f, 0.f);
+        // (at d = 64 the sums of the rounded values come from the tensor core)
+        uint32_t pk[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
+                                        c2, mneg2);
+            const float p0 = ex2_approx(x.x);
+            const float p1 = ex2_approx(x.y);
+            pk[c][i] = pack_bf16x2(p0, p1);
+            acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
+            if (!C::kSumByMma)
+              acc_mma[i & 3] = __fadd2_rn(acc_mma[i & 3], make_float2(__uint_as_float(pk[c][i] << 16),
+                                                                     __uint_as_float(pk[c][i] & 0xffff0000u)));
+          }
+        }
+        const float2 accs = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        const float2 accm = __fadd2_rn(__fadd2_rn(acc_mma[0], acc_mma[1]), __fadd2_rn(acc_mma[2], acc_mma[3]));
+        l = l * alpha + (accs.x + accs.y);
+        if (!C::kSumByMma) l_mma = l_mma * alpha + (accm.x + accm.y);
+        // P_t and O_t are in use until O_t += P_t(j-1) V_{j-1} has completed
+        // (at j = 0 the previous item's epilogue has already waited for its
+        // last product)
+        if (j > 0) {
+          if (!__all_sync(0xffffffffu, wait_bounded(&bar->pv_done[t], (uses - 1) & 1, ctx, kSiteFwdPvDone))) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        if (rescale_warp) {
+          // correction O <- alpha O, in place in tensor memory
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + 32 * c, ov);
+            tmem_wait_ld();
+            reg_fence32(ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(tO + 32 * c, ov);
+          }
+          if (C::kSumByMma) {
+            // the row sums of the rounded P are rescaled with O
+            uint32_t sv[16];
+            tmem_ld16(tO + D, sv);
+            tmem_wait_ld();
+            reg_fence16(sv);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sv[i] = __float_as_uint(__uint_as_float(sv[i]) * alpha);
+            tmem_st16(tO + D, sv);
+          }
+          tmem_wait_st();
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_st16(tP + 16 * c, pk[c]);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar->p_full[t]);
       }
+      if (!alive) break;
+      // epilogue: O = o / l_mma (at d = 64 from the extra O columns), LSE = (m + log2 l) ln 2.
+      // Once the tensor memory loads below have completed, the next item's
+      // first P V product may overwrite O_t (it is issued only after this
+      // warpgroup has written the next P_t).
+      if (!__all_sync(0xffffffffu, wait_bounded(&bar->pv_done[t], (uses - 1) & 1, ctx, kSiteFwdO))) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      if (C::kSumByMma) {
+        uint32_t sv[16];
+        tmem_ld16(tO + D, sv);
+        tmem_wait_ld();
+        reg_fence16(sv);
+        l_mma = __uint_as_float(sv[0]);
+      }
+      const float inv_l = 1.f / l_mma;
+      fwd_item<CAUSAL>(p, k, w);  // (recomputed rather than kept live through the loop)
+      __nv_bfloat16* orow = p.o + ((size_t)w.bh * N + row_g) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tO + 32 * c, ov);
+        tmem_wait_ld();
+        reg_fence32(ov);
+        if (row_g < N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 q4;
+            q4.x = pack_bf16x2(__uint_as_float(ov[8 * v4 + 0]) * inv_l, __uint_as_float(ov[8 * v4 + 1]) * inv_l);
+            q4.y = pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * inv_l, __uint_as_float(ov[8 * v4 + 3]) * inv_l);
+            q4.z = pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * inv_l, __uint_as_float(ov[8 * v4 + 5]) * inv_l);
+            q4.w = pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * inv_l, __uint_as_float(ov[8 * v4 + 7]) * inv_l);
+            dst[v4] = q4;
+          }
+        }
+      }
+      if (row_g < N) p.lse[(size_t)w.bh * N + row_g] = (m + log2f(l)) * 0.6931471805599453f;
+      tc_fence_before();
     }
   }
 

@@ -93,12 +93,25 @@ cudaError_t set_smem(Kernel kernel, int bytes) {
 }
 
 template <int D, bool CAUSAL>
-fa_status launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const fa::FwdParams& p,
+fa_status launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, fa::FwdParams p,
                      int BH, cudaStream_t stream) {
   using C = fa::FwdCfg<D>;
   auto kernel = fa::fa_fwd_kernel<D, CAUSAL>;
   if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
-  const long long grid = (long long)p.num_pairs * BH;
+  // persistent CTAs: one per SM (the kernel holds a whole SM), never more than there are items
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return FA_ERR_CUDA;
+  // Without the mask all pairs cost the same, and a last round of rem < sms
+  // pairs would keep the other SMs idle for a whole pair's time: when the
+  // pairs of that round fit on the SMs as single tiles, they run as single
+  // tiles.  (With the mask the last ranks are the lightest pairs already.)
+  const int pairs = p.num_pairs * BH;
+  const int rem = pairs % sms;
+  p.pair_items = (!CAUSAL && rem > 0 && 2 * rem <= sms) ? pairs - rem : pairs;
+  p.num_items = p.pair_items + 2 * (pairs - p.pair_items);
+  const long long grid = p.num_items < sms ? p.num_items : sms;
   const TimingEvents ev = timing_events();
   if (ev.fwd_start && ev.fwd_stop && cudaEventRecord(ev.fwd_start, stream) != cudaSuccess) return FA_ERR_CUDA;
   kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p);
@@ -281,6 +294,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.lse = lse;
   p.N = N;
   p.num_pairs = (N + 255) / 256;
+  p.num_bh = BH;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = wait_limit_ns();
   p.debug_stall = g_debug_stall.load();
