@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(256)
 // number of 128-row blocks (Npad = 128 ceil(N / 128)):
 //   delta_pad[bh][n] = sum_c dO_nc O_nc      (0 for n >= N)
 //   lse2_pad[bh][n]  = LSE_n * log2(e)       (+inf for n >= N, so P = 0 there)
-// and the fp32 dQ accumulator rows are zeroed.  The padded, 128-aligned rows
+// and the fp32 dQ accumulator rows are zeroed (when there is one).  The padded, 128-aligned rows
 // let the main kernel bring both vectors in with TMA next to each Q tile.
 // ---------------------------------------------------------------------------
 template <int D>
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(256)
       delta_pad[prow] = valid ? s : 0.f;
       lse2_pad[prow] = valid ? __ldg(lse + row) * 1.4426950408889634f : CUDART_INF_F;
     }
-    if (valid) {
+    if (valid && dq_acc) {
       float4* z = reinterpret_cast<float4*>(dq_acc + row * D) + 2 * sub;
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -162,11 +162,15 @@ __global__ void __launch_bounds__(256)
 constexpr uint32_t kBwdWorkRegs = 144, kBwdMiscRegs = 80;
 static_assert(3 * kBwdWorkRegs + kBwdMiscRegs == 4 * 128, "register split must match the launch budget");
 
-template <int D>
+// kAtomicDq: the kernel also forms dQ_i = dS K_j and adds it into the fp32
+// accumulator (reducer warps); otherwise dQ is left to the separate
+// deterministic pass, and the shared memory of the reducers' staging tiles
+// goes to a fourth ring slot at d = 128.
+template <int D, bool kAtomicDq>
 struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kAtoms = D / 64;
-  static constexpr int kSlots = (D == 128) ? 3 : 6;   // Q / dO ring
+  static constexpr int kSlots = (D == 128) ? (kAtomicDq ? 3 : 4) : 6;   // Q / dO ring
   static constexpr int kStatBytes = 1024;             // LSE*log2e and delta of one query block
   // one entry per query block whose statistics can be in use or in flight.
   // Q_i (and its statistics) is loaded once the slot of fill 2i - kSlots is
@@ -177,7 +181,7 @@ struct BwdCfg {
   // reads delta) has finished: one entry more.
   static constexpr int kStatEntries = (kSlots % 2) ? (kSlots + 1) / 2 + 1 : kSlots / 2;
   static constexpr int kDsBytes = 128 * 128 * 2;      // dS^T tile: 2 atom columns of 64 queries
-  static constexpr int kStageBytes = 4 * 4096;        // reducers' transposing tiles
+  static constexpr int kStageBytes = kAtomicDq ? 4 * 4096 : 0;  // reducers' transposing tiles
   static constexpr int kThreads = 512;
   static constexpr int kLaunchRegs = 128;             // 65536 / 512
   static constexpr uint32_t kTmemCols = 512;
@@ -214,13 +218,13 @@ struct BwdParams {
 enum : int { kSiteBwdProducer = 16, kSiteBwdKV, kSiteBwdQ, kSiteBwdDo, kSiteBwdDvDone, kSiteBwdDqFree, kSiteBwdEw,
              kSiteBwdS, kSiteBwdDp, kSiteBwdDq, kSiteBwdAcc };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool kAtomicDq>
 __global__ void __launch_bounds__(512, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                   const __grid_constant__ CUtensorMap map_lse2, const __grid_constant__ CUtensorMap map_delta,
                   const BwdParams p) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, kAtomicDq>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {
     // the 128-byte-swizzled tiles need 1024-byte alignment: report, do nothing
@@ -365,10 +369,15 @@ __global__ void __launch_bounds__(512, 1)
               mma_commit(&bar->s_full);
             } else {
               // dP^T = V dO_i^T, once the reducers have taken the previous dQ
-              // out of these columns
+              // out of these columns (without dQ: once the elementwise step
+              // has read the previous dP^T)
               const int fd = 2 * it + 1, sd = fd % C::kSlots;
               if (!wait_bounded_inl(&bar->ring_full[sd], (fd / C::kSlots) & 1, ctx, kSiteBwdDo)) { ok = false; break; }
-              if (it > 0 && !wait_bounded_inl(&bar->dq_free, (it - 1) & 1, ctx, kSiteBwdDqFree)) { ok = false; break; }
+              if (it > 0 && !wait_bounded_inl(kAtomicDq ? &bar->dq_free : &bar->ew_done, (it - 1) & 1, ctx,
+                                              kSiteBwdDqFree)) {
+                ok = false;
+                break;
+              }
               tc_fence_after();
               const uint64_t dodesc = sdesc_sw128(ring + sd * C::kTileBytes, 16, 1024);
 #pragma unroll
@@ -426,11 +435,13 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int step = 0; step < 2; ++step) {
             if ((step == 0) == kDqFirst) {
+              if (kAtomicDq) {
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4),
-                            id_q, kk > 0 ? 1u : 0u);
-              mma_commit(&bar->dq_full);
+                for (int kk = 0; kk < 8; ++kk)
+                  mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4),
+                              id_q, kk > 0 ? 1u : 0u);
+                mma_commit(&bar->dq_full);
+              }
             } else {
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
@@ -455,6 +466,8 @@ __global__ void __launch_bounds__(512, 1)
     // warp 15 has no role
   } else if (warp >= 8) {
     // ------------------------------------------------------------------ reducers
+    // (no role without the atomic dQ: the warpgroup keeps its launch budget)
+    if (kAtomicDq) {
     setmaxnreg_inc<kBwdWorkRegs>();
     const int q = warp & 3;
     const uint32_t tDQ = tmem + C::kDpCol + ((uint32_t)(q * 32) << 16);
@@ -493,6 +506,7 @@ __global__ void __launch_bounds__(512, 1)
         }
         __syncwarp();
       }
+    }
     }
   } else {
     // ------------------------------------------------------------------ elementwise

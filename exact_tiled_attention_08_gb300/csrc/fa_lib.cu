@@ -17,6 +17,7 @@
 #include "sm103_ptx.cuh"
 #include "fa_fwd.cuh"
 #include "fa_bwd.cuh"
+#include "fa_bwd_dq.cuh"
 
 namespace {
 
@@ -120,10 +121,10 @@ fa_status launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   return FA_OK;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool ATOMIC_DQ>
 fa_status launch_bwd(const CUtensorMap* maps, const fa::BwdParams& p, int BH, cudaStream_t stream) {
-  using C = fa::BwdCfg<D>;
-  auto kernel = fa::fa_bwd_kernel<D, CAUSAL>;
+  using C = fa::BwdCfg<D, ATOMIC_DQ>;
+  auto kernel = fa::fa_bwd_kernel<D, CAUSAL, ATOMIC_DQ>;
   if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
   // the kernel's warpgroups re-divide the registers the block launches with
   // (setmaxnreg); that only works if the block really gets 128 per thread
@@ -137,6 +138,16 @@ fa_status launch_bwd(const CUtensorMap* maps, const fa::BwdParams& p, int BH, cu
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_stop, stream) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
+}
+
+template <int D, bool CAUSAL>
+fa_status launch_bwd_dq(const CUtensorMap* maps, const fa::BwdDqParams& p, int BH, cudaStream_t stream) {
+  using C = fa::BwdDqCfg<D>;
+  auto kernel = fa::fa_bwd_dq_kernel<D, CAUSAL>;
+  if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
+  const long long grid = (long long)p.nqb * BH;
+  kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 // fp32 [rows][cols] viewed as a 2-D tensor (cols, rows); boxes of box_cols x 1, no swizzle
@@ -168,14 +179,16 @@ struct BwdWorkspace {
 };
 
 // The backward pass proper, given device scratch of BwdWorkspace::total() bytes.
+// deterministic: dQ by the separate query-major pass instead of fp32 atomics
+// (the dQ accumulator part of the scratch is then not used).
 fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                   void* dq, void* dk, void* dv, void* scratch, int B, int H, int N, int d, float scale, int causal,
-                  cudaStream_t stream) {
+                  bool deterministic, cudaStream_t stream) {
   const int BH = B * H;
   const int nkb = (N + 127) / 128;
   const int npad = nkb * 128;
   const BwdWorkspace w = BwdWorkspace::of(B, H, N, d);
-  float* dq_acc = static_cast<float*>(scratch);
+  float* dq_acc = deterministic ? nullptr : static_cast<float*>(scratch);
   float* delta_pad = reinterpret_cast<float*>(static_cast<char*>(scratch) + w.dq_bytes);
   float* lse2_pad = reinterpret_cast<float*>(static_cast<char*>(scratch) + w.dq_bytes + w.stat_bytes);
   CUtensorMap maps[6];
@@ -183,7 +196,7 @@ fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, co
       !encode_bhnd(&maps[2], v, BH, N, d) || !encode_bhnd(&maps[3], dout, BH, N, d) ||
       !encode_f32_rows(&maps[4], lse2_pad, BH, npad, 128) || !encode_f32_rows(&maps[5], delta_pad, BH, npad, 128))
     return FA_ERR_CUDA;
-  // 1. delta, LSE*log2(e) (padded), dQ accumulator = 0
+  // 1. delta, LSE*log2(e) (padded), dQ accumulator = 0 (atomic dQ only)
   {
     const long long padded_rows = (long long)BH * npad;
     const long long per_block = 256 / (d / 8);
@@ -199,7 +212,7 @@ fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, co
           dq_acc, N, npad, padded_rows);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   }
-  // 2. dK, dV and the fp32 dQ accumulation
+  // 2. dK, dV (and the fp32 dQ accumulation)
   fa::BwdParams p;
   p.dq_acc = dq_acc;
   p.dk_out = static_cast<__nv_bfloat16*>(dk);
@@ -211,10 +224,31 @@ fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, co
   p.wait_limit_ns = wait_limit_ns();
   p.debug_stall = g_debug_stall.load();
   fa_status st;
+  if (deterministic) {
+    if (d == 128)
+      st = causal ? launch_bwd<128, true, false>(maps, p, BH, stream) : launch_bwd<128, false, false>(maps, p, BH, stream);
+    else
+      st = causal ? launch_bwd<64, true, false>(maps, p, BH, stream) : launch_bwd<64, false, false>(maps, p, BH, stream);
+    if (st != FA_OK) return st;
+    // 3'. dQ by the query-major pass, written once as bf16
+    fa::BwdDqParams pq;
+    pq.delta_pad = delta_pad;
+    pq.lse2_pad = lse2_pad;
+    pq.dq = static_cast<__nv_bfloat16*>(dq);
+    pq.N = N;
+    pq.nqb = nkb;
+    pq.scale_log2 = p.scale_log2;
+    pq.scale = scale;
+    pq.wait_limit_ns = p.wait_limit_ns;
+    pq.debug_stall = p.debug_stall;
+    if (d == 128)
+      return causal ? launch_bwd_dq<128, true>(maps, pq, BH, stream) : launch_bwd_dq<128, false>(maps, pq, BH, stream);
+    return causal ? launch_bwd_dq<64, true>(maps, pq, BH, stream) : launch_bwd_dq<64, false>(maps, pq, BH, stream);
+  }
   if (d == 128)
-    st = causal ? launch_bwd<128, true>(maps, p, BH, stream) : launch_bwd<128, false>(maps, p, BH, stream);
+    st = causal ? launch_bwd<128, true, true>(maps, p, BH, stream) : launch_bwd<128, false, true>(maps, p, BH, stream);
   else
-    st = causal ? launch_bwd<64, true>(maps, p, BH, stream) : launch_bwd<64, false>(maps, p, BH, stream);
+    st = causal ? launch_bwd<64, true, true>(maps, p, BH, stream) : launch_bwd<64, false, true>(maps, p, BH, stream);
   if (st != FA_OK) return st;
   // 3. dQ = scale * dQ_acc -> bf16
   const long long n8 = (long long)BH * N * d / 8;
@@ -327,7 +361,21 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
     return FA_ERR_MISALIGNED;
-  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, H, N, d, scale, causal, stream);
+  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, H, N, d, scale, causal, false, stream);
+}
+
+fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                               const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                               int B, int H, int N, int d, float scale, int causal, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+  fa_status st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale, causal)) != FA_OK) return st;
+  if (ws_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return FA_ERR_MISALIGNED;
+  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, H, N, d, scale, causal, true, stream);
 }
 
 }  // extern "C"
@@ -389,7 +437,7 @@ fa_status fa_bwd_static_scratch(const void* q, const void* k, const void* v, con
   if ((st = static_scratch_on_current_device(&scratch)) != FA_OK) return st;
   // the previous call's contents stay in the array: the preprocess rewrites
   // delta and LSE*log2(e) and zeroes the dQ accumulator before anything reads them
-  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch, B, H, N, d, scale, causal, stream);
+  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch, B, H, N, d, scale, causal, false, stream);
 }
 
 }  // extern "C"

@@ -61,6 +61,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_bwd_workspace_bytes.restype = sz
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, vp]
+    lib.fa_bwd_deterministic.restype = i
     lib.fa_bwd_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_bwd_static_scratch.restype = i
     lib.fa_check_device_status.argtypes = [vp]
@@ -170,8 +172,7 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(load_library().fa_bwd_workspace_bytes(B, H, N, d))
 
 
-def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: bool, stream=None) -> None:
-    """dQ, dK, dV of attention by recomputation; workspace is a uint8 device tensor."""
+def _bwd_call(entry: str, q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: bool, stream):
     B, H, N, d = _shape4(q, "q")
     dev = q.device
     for t, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
@@ -180,10 +181,22 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: b
     if workspace.device != dev or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous tensor on the inputs' device")
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = load_library().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
-                               lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
-                               ws_bytes, B, H, N, d, float(scale), int(bool(causal)), _stream_handle(stream))
-    _raise(st, "fa_bwd")
+    st = getattr(load_library(), entry)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                        workspace.data_ptr(), ws_bytes, B, H, N, d, float(scale),
+                                        int(bool(causal)), _stream_handle(stream))
+    _raise(st, entry)
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: bool, stream=None) -> None:
+    """dQ, dK, dV of attention by recomputation; workspace is a uint8 device tensor."""
+    _bwd_call("fa_bwd", q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, stream)
+
+
+def fa_bwd_deterministic(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: bool,
+                         stream=None) -> None:
+    """fa_bwd with dQ summed by a separate query-major pass: bitwise repeatable."""
+    _bwd_call("fa_bwd_deterministic", q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, stream)
 
 
 FA_STATIC_SCRATCH_BYTES = 72 * 1024 * 1024
@@ -216,10 +229,12 @@ def attention_forward(q, k, v, scale: float, causal: bool = False, stream=None):
     return o, lse
 
 
-def attention_backward(q, k, v, o, dout, lse, scale: float, causal: bool = False, workspace=None, stream=None):
+def attention_backward(q, k, v, o, dout, lse, scale: float, causal: bool = False, workspace=None, stream=None,
+                       deterministic: bool = False):
     B, H, N, d = _shape4(q, "q")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
         workspace = torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
-    fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, stream)
+    (fa_bwd_deterministic if deterministic else fa_bwd)(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal,
+                                                        stream)
     return dq, dk, dv

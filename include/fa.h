@@ -120,6 +120,25 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, cudaStream_t stream);
 
 /*
+ * Backward pass with a deterministic dQ.  Same arguments, layout, workspace
+ * (ws_bytes >= fa_bwd_workspace_bytes()) and error behaviour as fa_bwd, and
+ * the same dQ, dK, dV up to rounding; dQ, dK and dV are bitwise repeatable
+ * from run to run on the same device.  "Interrogating the GPU part 5:
+ * FlashAttention", section "What does the backward pass do without P?"
+ * (recompute formula, dS = P o (dP - delta)); dQ accumulated in fp32 "by a
+ * separate pass" rather than atomically: after the key-block-major pass that
+ * forms dK and dV, a query-block-major pass recomputes S = Q K^T,
+ * dP = dO V^T and dS for each of its query blocks, sums dQ = scale dS K over
+ * the key blocks in a fixed order in tensor memory, and writes it once.
+ * This costs three more N x N x d products per head pair (the backward does
+ * 7 N^2 d multiply-adds per (batch, head) instead of 5) and needs no fp32
+ * atomics; the dQ accumulator part of the workspace is not used.
+ */
+fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                               const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                               int B, int H, int N, int d, float scale, int causal, cudaStream_t stream);
+
+/*
  * Backward pass with library-owned scratch.  This entry point has no
  * counterpart on the source pages; it exists for callers that cannot
  * allocate device memory when they run the backward pass -- for example a

@@ -72,23 +72,24 @@ def test_fwd_validation(lib):
     assert fwd(lib, lse=P + 4) == fa.FA_ERR_MISALIGNED
 
 
-def bwd(lib, ws_bytes=None, ws=P, dq=P, B=1, H=1, N=128, d=128, scale=0.1, causal=0):
+def bwd(lib, ws_bytes=None, ws=P, dq=P, B=1, H=1, N=128, d=128, scale=0.1, causal=0, entry="fa_bwd"):
     if ws_bytes is None:
         ws_bytes = lib.fa_bwd_workspace_bytes(B, H, N, d)
-    return lib.fa_bwd(VP(P), VP(P), VP(P), VP(P), VP(P), VP(P), VP(dq), VP(P), VP(P), VP(ws), ws_bytes,
-                      B, H, N, d, scale, causal, None)
+    return getattr(lib, entry)(VP(P), VP(P), VP(P), VP(P), VP(P), VP(P), VP(dq), VP(P), VP(P), VP(ws), ws_bytes,
+                               B, H, N, d, scale, causal, None)
 
 
-def test_bwd_validation(lib):
-    assert bwd(lib, ws=0) == fa.FA_ERR_INVALID_ARG
-    assert bwd(lib, dq=0) == fa.FA_ERR_INVALID_ARG
-    assert bwd(lib, d=32) == fa.FA_ERR_UNSUPPORTED
-    assert bwd(lib, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
-    assert bwd(lib, causal=-1) == fa.FA_ERR_INVALID_ARG
+@pytest.mark.parametrize("entry", ["fa_bwd", "fa_bwd_deterministic"])
+def test_bwd_validation(lib, entry):
+    assert bwd(lib, ws=0, entry=entry) == fa.FA_ERR_INVALID_ARG
+    assert bwd(lib, dq=0, entry=entry) == fa.FA_ERR_INVALID_ARG
+    assert bwd(lib, d=32, entry=entry) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(lib, scale=float("nan"), entry=entry) == fa.FA_ERR_INVALID_ARG
+    assert bwd(lib, causal=-1, entry=entry) == fa.FA_ERR_INVALID_ARG
     need = lib.fa_bwd_workspace_bytes(1, 1, 128, 128)
-    assert bwd(lib, ws_bytes=need - 1) == fa.FA_ERR_INVALID_ARG
-    assert bwd(lib, dq=BAD) == fa.FA_ERR_MISALIGNED
-    assert bwd(lib, ws=BAD) == fa.FA_ERR_MISALIGNED
+    assert bwd(lib, ws_bytes=need - 1, entry=entry) == fa.FA_ERR_INVALID_ARG
+    assert bwd(lib, dq=BAD, entry=entry) == fa.FA_ERR_MISALIGNED
+    assert bwd(lib, ws=BAD, entry=entry) == fa.FA_ERR_MISALIGNED
 
 
 def test_preprocess_validation(lib):
