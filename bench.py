@@ -57,6 +57,8 @@ def parse_args():
                     help="head chunks pipelined over copy-in / compute / copy-out streams in the end-to-end leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="backward by fa_bwd_deterministic (dQ by the separate query-major pass, no atomics)")
     return ap.parse_args()
 
 
@@ -296,10 +298,14 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.Stream(device=dev)
     fwd_flops, bwd_flops = w.fwd_flops(), w.bwd_flops()
     step_flops = fwd_flops + bwd_flops
+    bwd_entry = fa.fa_bwd_deterministic if args.deterministic else fa.fa_bwd
+    # the main backward kernel does all five products, or four of them when dQ
+    # is left to the deterministic pass (whose time is then in "other_ms")
+    bwd_main_flops = bwd_flops * (0.8 if args.deterministic else 1.0)
 
     def step():
         fa.fa_fwd(q, k, v, o, lse, scale, w.causal, stream)
-        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, w.causal, stream)
+        bwd_entry(q, k, v, o, do, lse, dq, dk, dv, ws, scale, w.causal, stream)
 
     K, W = args.steps, args.warmup
     with torch.cuda.stream(stream):
@@ -384,7 +390,7 @@ def run_ours(args, rank, world, local):
                 qc, kc, vc, doc = (heads(d_in[x], lo, hi) for x in ("q", "k", "v", "do"))
                 oc, lc = heads(o, lo, hi), heads(lse, lo, hi)
                 fa.fa_fwd(qc, kc, vc, oc, lc, scale, w.causal, stream)
-                fa.fa_bwd(qc, kc, vc, oc, doc, lc, heads(dq, lo, hi), heads(dk, lo, hi), heads(dv, lo, hi), ws, scale,
+                bwd_entry(qc, kc, vc, oc, doc, lc, heads(dq, lo, hi), heads(dk, lo, hi), heads(dv, lo, hi), ws, scale,
                           w.causal, stream)
                 done = torch.cuda.Event()
                 done.record(stream)
@@ -408,7 +414,7 @@ def run_ours(args, rank, world, local):
         return
     peaks, peak_source = load_peaks()
     fwd_tf = fwd_flops / (fwd_ms / 1e3) / 1e12
-    bwd_tf = bwd_flops / (bwd_ms / 1e3) / 1e12
+    bwd_tf = bwd_main_flops / (bwd_ms / 1e3) / 1e12
     # dominant kernel: the one with the larger share of the step
     if bwd_ms >= fwd_ms:
         dom, dom_tf, dom_name = "bwd", bwd_tf, "fa_bwd_kernel"
@@ -416,7 +422,8 @@ def run_ours(args, rank, world, local):
         dom, dom_tf, dom_name = "fwd", fwd_tf, "fa_fwd_kernel"
     peak = peaks["bf16_tflops_sustained"]
     roofline = {"bound": "tensor", "achieved": dom_tf, "peak": peak, "unit": "TFLOP/s", "frac": dom_tf / peak,
-                "traffic": recorded_traffic(dom_name, w.name), "kernel": dom_name,
+                "traffic": recorded_traffic(dom_name + ("/deterministic" if args.deterministic and dom == "bwd" else ""),
+                                            w.name), "kernel": dom_name,
                 "peak_source": f"{peak_source} bf16 sustained (kernel timed inside a long run of steps)",
                 "frac_of_burst_peak": dom_tf / peaks["bf16_tflops"]}
     line = {
@@ -425,7 +432,8 @@ def run_ours(args, rank, world, local):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "l2": "flushed before every timed step (256 MiB write, outside the step's events)",
-                   "step": "fa_fwd + fa_bwd (preprocess, main kernel, dQ cast)",
+                   "step": ("fa_fwd + fa_bwd_deterministic (preprocess, dK/dV kernel, dQ pass)" if args.deterministic
+                            else "fa_fwd + fa_bwd (preprocess, main kernel, dQ cast)"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
         "breakdown": {"fwd_kernel_ms": fwd_ms, "fwd_tflops": fwd_tf, "bwd_kernel_ms": bwd_ms, "bwd_tflops": bwd_tf,

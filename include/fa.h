@@ -125,8 +125,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * the same dQ, dK, dV up to rounding; dQ, dK and dV are bitwise repeatable
  * from run to run on the same device.  "Interrogating the GPU part 5:
  * FlashAttention", section "What does the backward pass do without P?"
- * (recompute formula, dS = P o (dP - delta)); dQ accumulated in fp32 "by a
- * separate pass" rather than atomically: after the key-block-major pass that
+ * (recompute formula, dS = P o (dP - delta)); "LLM Flash Attention", section
+ * "End-to-end flow" (each recomputed block contributes to the gradients; how
+ * the contributions to dQ are summed is left open).  Here they are summed by a
+ * separate pass rather than with atomics: after the key-block-major pass that
  * forms dK and dV, a query-block-major pass recomputes S = Q K^T,
  * dP = dO V^T and dS for each of its query blocks, sums dQ = scale dS K over
  * the key blocks in a fixed order in tensor memory, and writes it once.
