@@ -346,20 +346,25 @@ def run_ours(args, rank, world, local):
     step_ms_max = max_over_ranks(step_ms, world)
     value = world * step_flops / (step_ms_max / 1e3) / 1e12
 
-    # ---- end to end through the C ABI with pinned host buffers.  The heads
-    # are split into chunks (every tensor is laid out head-major, so a range of
-    # heads is a contiguous slice) and pipelined over three streams: while
-    # chunk c is computed, chunk c+1's inputs come in and chunk c-1's results
-    # go out.  Each chunk is one fa_fwd + fa_bwd call on its heads.
+    # ---- end to end through the C ABI with pinned host buffers.  Every step
+    # copies its inputs (Q, K, V, dO) from pinned host memory to the device and
+    # its results (O, LSE, dQ, dK, dV) back, inside the timed region.  The
+    # heads are split into chunks (every tensor is laid out head-major, so a
+    # range of heads is a contiguous slice) and the work is pipelined over
+    # three streams, within a step and across steps: the device tensors are
+    # double-buffered by step parity, so while step i is computed, step i+1's
+    # inputs come in and step i-1's results go out.  Each chunk is one
+    # fa_fwd + fa_bwd call on its heads.
     o_ref = o.clone()
     h_in = {x: inp_cpu[x].pin_memory() for x in ("q", "k", "v", "do")}
     h_out = {"o": torch.empty_like(o, device="cpu").pin_memory(), "lse": torch.empty_like(lse, device="cpu").pin_memory(),
              "dq": torch.empty_like(dq, device="cpu").pin_memory(), "dk": torch.empty_like(dk, device="cpu").pin_memory(),
              "dv": torch.empty_like(dv, device="cpu").pin_memory()}
-    d_in = {"q": q, "k": k, "v": v, "do": do}
-    d_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    sets = [({"q": q, "k": k, "v": v, "do": do}, {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv})]
+    sets.append(({x: torch.empty_like(t) for x, t in sets[0][0].items()},
+                 {x: torch.empty_like(t) for x, t in sets[0][1].items()}))
     BH = w.B * w.H
     chunks = max(1, min(args.e2e_chunks, BH))
     bounds = [(c * BH // chunks, (c + 1) * BH // chunks) for c in range(chunks)]
@@ -369,45 +374,59 @@ def run_ours(args, rank, world, local):
         return t.view(1, BH, *t.shape[2:])[:, lo:hi]
 
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    E = max(1, args.e2e_steps)
-    e2e_ev = []
-    prev_end = None
-    for i in range(E + 3):
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if prev_end is not None:
-            s_in.wait_event(prev_end)
-        s0.record(s_in)
-        stream.wait_event(s0)
-        s_out.wait_event(s0)
-        for lo, hi in bounds:
+    # per (buffer set, chunk): inputs consumed by the compute, results copied out
+    consumed = [[None] * chunks for _ in range(2)]
+    copied_out = [[None] * chunks for _ in range(2)]
+
+    def e2e_step(i):
+        d_in, d_out = sets[i % 2]
+        for c, (lo, hi) in enumerate(bounds):
             with torch.cuda.stream(s_in):
+                if consumed[i % 2][c] is not None:
+                    s_in.wait_event(consumed[i % 2][c])
                 for name, t in d_in.items():
                     heads(t, lo, hi).copy_(heads(h_in[name], lo, hi), non_blocking=True)
                 got_in = torch.cuda.Event()
                 got_in.record(s_in)
             stream.wait_event(got_in)
+            if copied_out[i % 2][c] is not None:
+                stream.wait_event(copied_out[i % 2][c])
             with torch.cuda.stream(stream):
                 qc, kc, vc, doc = (heads(d_in[x], lo, hi) for x in ("q", "k", "v", "do"))
-                oc, lc = heads(o, lo, hi), heads(lse, lo, hi)
+                oc, lc = heads(d_out["o"], lo, hi), heads(d_out["lse"], lo, hi)
                 fa.fa_fwd(qc, kc, vc, oc, lc, scale, w.causal, stream)
-                bwd_entry(qc, kc, vc, oc, doc, lc, heads(dq, lo, hi), heads(dk, lo, hi), heads(dv, lo, hi), ws, scale,
-                          w.causal, stream)
+                bwd_entry(qc, kc, vc, oc, doc, lc, heads(d_out["dq"], lo, hi), heads(d_out["dk"], lo, hi),
+                          heads(d_out["dv"], lo, hi), ws, scale, w.causal, stream)
                 done = torch.cuda.Event()
                 done.record(stream)
+            consumed[i % 2][c] = done
             s_out.wait_event(done)
             with torch.cuda.stream(s_out):
                 for name, t in h_out.items():
                     heads(t, lo, hi).copy_(heads(d_out[name], lo, hi), non_blocking=True)
-        s1.record(s_out)
-        prev_end = s1
-        if i >= 3:
-            e2e_ev.append((s0, s1))
+                out_ev = torch.cuda.Event()
+                out_ev.record(s_out)
+            copied_out[i % 2][c] = out_ev
+
+    E = max(1, args.e2e_steps)
+    for i in range(3):  # warm-up
+        e2e_step(i)
     torch.cuda.synchronize(dev)
+    barrier(world)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(s_in)
+    for i in range(3, 3 + E):
+        e2e_step(i)
+    s_out.wait_stream(stream)
+    s_out.wait_stream(s_in)
+    t_end.record(s_out)
+    torch.cuda.synchronize(dev)
+    barrier(world)
     assert fa.fa_check_device_status(stream) == fa.FA_OK
     # the pipelined run computed exactly what the device-resident one did
     if not torch.equal(h_out["o"], o_ref.cpu()):
         raise SystemExit("bench.py: end-to-end outputs differ from the device-resident run")
-    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), world)
+    e2e_ms = max_over_ranks(t_start.elapsed_time(t_end) / E, world)
     e2e_value = world * step_flops / (e2e_ms / 1e3) / 1e12
 
     if rank != 0:
@@ -440,7 +459,9 @@ def run_ours(args, rank, world, local):
                       "other_ms": step_ms - fwd_ms - bwd_ms,
                       "fwd_frac_of_sustained_peak": fwd_tf / peak, "bwd_frac_of_sustained_peak": bwd_tf / peak},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms, "chunks": chunks},
+                "ms_per_step": e2e_ms, "chunks": chunks, "steps": E,
+                "pipelining": "head chunks over copy-in/compute/copy-out streams; device buffers double-buffered "
+                              "by step parity, so step i+1's inputs and step i-1's results move during step i"},
         "gpu_launches": 4 * K,
         "clocks": clock_info,
     }
