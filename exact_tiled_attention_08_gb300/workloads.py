@@ -91,3 +91,25 @@ def workload_inputs(w: Workload, with_dout: bool = True) -> dict:
 def to_f32_numpy(t: torch.Tensor):
     """Exact widening of a (bf16) tensor to a float32 numpy array on the host."""
     return t.detach().to("cpu", torch.float32).numpy()
+
+
+def rotation_signs(d: int, seed: int) -> torch.Tensor:
+    """d random signs (+1 / -1, int8) for the FP8 forward's Hadamard rotation."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    return (torch.randint(0, 2, (d,), generator=gen, dtype=torch.int8) * 2 - 1).to(torch.int8)
+
+
+def make_outlier_inputs(B: int, H: int, N: int, d: int, seed: int, frac: float = 1e-3,
+                        outlier_std: float = 10.0) -> dict:
+    """bf16 ``q, k, v`` whose entries are N(0, 1) plus, with probability
+    ``frac``, an extra N(0, outlier_std^2): a few large entries scattered over
+    the tensors, the case per-tensor FP8 scaling handles badly."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    shape = (B, H, N, d)
+    out = {}
+    for name in ("q", "k", "v"):
+        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        hit = torch.rand(shape, generator=gen) < frac
+        x = x + hit * outlier_std * torch.randn(shape, generator=gen, dtype=torch.float32)
+        out[name] = x.to(torch.bfloat16)
+    return out

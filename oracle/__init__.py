@@ -15,10 +15,13 @@ Every function cites the passage of the source pages it follows:
 * "FlashAttention" (datarekha.com), cited as [datarekha];
 * "LLM Flash Attention" (aicassindra.com), cited as [aicassindra].
 
-Parity status: every function here is pinned by ``tests/test_oracle.py``
-(closed forms, invariants, a pure-Python brute force, finite differences and
-the worked example that [datarekha] prints).  No function is "parity
-unpinned".
+Parity status: every function in ``attention`` is pinned by
+``tests/test_oracle.py`` (closed forms, invariants, a pure-Python brute
+force, finite differences and the worked example that [datarekha] prints),
+and every function in ``fp8`` (the FP8 forward's rotation, E4M3 rounding and
+block quantisation) by ``tests/test_oracle_fp8.py`` (torch's float8 cast, the
+format's codes, closed forms, orthogonality, error bounds and the direction
+of the pages' error claim).  No function is "parity unpinned".
 """
 
 from .attention import (  # noqa: F401
