@@ -54,33 +54,47 @@ constexpr float kRescaleThresholdLog2 = 8.0f;
 
 constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;  // waits while draining after an abort
 
-template <int D>
+// FP8: the E4M3 variant of the same kernel (fa_fwd_fp8): Q and K arrive
+// rotated and quantised per 128-row block, V quantised per channel and stored
+// transposed per key block (d rows of 128 keys, K-major), P is rounded to E4M3
+// for the P V product, and the per-block and per-channel scales are applied to
+// the scores and to O.
+template <int D, bool FP8 = false>
 struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
+  static_assert(!FP8 || D == 128, "the FP8 forward is built for d = 128");
   static constexpr int kTileRows = 128;
-  static constexpr int kTileBytes = kTileRows * D * 2;  // Q, K, V tiles
-  static constexpr int kAtoms = D / 64;                 // 64-column atom columns per tile
+  static constexpr int kElemBytes = FP8 ? 1 : 2;
+  static constexpr int kTileBytes = kTileRows * D * kElemBytes;  // Q, K, V tiles
+  static constexpr int kAtoms = D * kElemBytes / 128;             // 128-byte atom columns per tile
+  static constexpr int kAtomElems = 128 / kElemBytes;             // elements per atom row
+  static constexpr int kKSteps = D * kElemBytes / 32;             // MMAs of the S product (32 bytes of K each)
   static constexpr int kThreads = 352;
   static constexpr uint32_t kTmemCols = 512;
-  // At d = 64 the tensor core also forms the row sums of the bf16 P that the
-  // output product uses: each V tile in the ring is followed by a tile of ones,
-  // the product O += P [V | 1] is 16 columns wider, and those columns hold
-  // sum_k P_rk, rescaled together with O.  At d = 128 the columns are not
-  // there (S 128 + P 2 x 64 + O 2 x 128 = 512) and the softmax sums them.
-  static constexpr bool kSumByMma = (D == 64);
+  // At d = 64 (and in FP8) the tensor core also forms the row sums of the
+  // rounded P that the output product uses: each V operand in the ring is
+  // followed by ones, the product O += P [V | 1] is 16 columns wider, and
+  // those columns hold sum_k P_rk, rescaled together with O.  bf16 d = 64:
+  // V is read N-major and the ones are a 64-column atom of bf16 ones after it;
+  // FP8: V^T is read K-major and the ones are 16 more rows of E4M3 ones.  At
+  // bf16 d = 128 the columns are not there (S 128 + P 2 x 64 + O 2 x 128 =
+  // 512) and the softmax sums the rounded values itself.
+  static constexpr bool kSumByMma = FP8 || (D == 64);
   static constexpr int kOCols = kSumByMma ? D + 16 : D;  // O accumulator columns
-  static constexpr int kOnesBytes = kSumByMma ? 16384 : 0;
+  static constexpr int kOnesBytes = FP8 ? 16 * 128 : (kSumByMma ? 16384 : 0);
   // K_j is ring fill 2j, V_j fill 2j+1; with the ones tiles the slots come in
   // pairs (K, V, ones), so the slot count is even
-  static constexpr int kSlots = (D == 128) ? 5 : 8;
+  static constexpr int kSlots = FP8 ? 10 : ((D == 128) ? 5 : 8);
   static_assert(!kSumByMma || kSlots % 2 == 0, "K/V slot pairs");
   static constexpr int kStageBytes = 2 * kTileBytes + kOnesBytes;
   static constexpr int kRingBytes = kSumByMma ? (kSlots / 2) * kStageBytes : kSlots * kTileBytes;
   static __device__ __host__ constexpr int slot_offset(int s) {
     return kSumByMma ? (s / 2) * kStageBytes + (s & 1) * kTileBytes : s * kTileBytes;
   }
-  static constexpr uint32_t kSCol = 0, kPCol0 = 128, kPCol1 = 192;
-  static constexpr uint32_t kOCol0 = 256, kOCol1 = 256 + kOCols;
+  // P of one tile: 128 keys, two bf16 or four E4M3 per column
+  static constexpr uint32_t kPCols = FP8 ? 32 : 64;
+  static constexpr uint32_t kSCol = 0, kPCol0 = 128, kPCol1 = 128 + kPCols;
+  static constexpr uint32_t kOCol0 = 128 + 2 * kPCols, kOCol1 = kOCol0 + kOCols;
   static_assert(kOCol1 + kOCols <= kTmemCols, "tensor memory budget");
   static constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kRingBytes + 512;
 };
@@ -111,6 +125,11 @@ struct FwdParams {
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
   int debug_stall;  // nonzero: the MMA thread first waits on `never` (tests the timeout path)
+  // FP8 only: dequantisation scales
+  const float* q_scale;  // [B*H][nkb]: query block scales
+  const float* k_scale;  // [B*H][nkb]: key block scales
+  const float* v_scale;  // [B*H][D]: value channel scales
+  int nkb;               // 128-row blocks per head
 };
 
 // wait sites reported in the status word
@@ -167,11 +186,11 @@ __device__ __forceinline__ bool fwd_item(const FwdParams& p, int k, FwdItem& w) 
   return true;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool FP8 = false>
 __global__ void __launch_bounds__(352, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -182,10 +201,11 @@ __global__ void __launch_bounds__(352, 1)
   const int N = p.N;
 
   if (C::kSumByMma) {
-    // the ones tiles (bf16 1.0) after each V slot, read by the tensor core
+    // the ones after each V slot (bf16 1.0 = 0x3f80, E4M3 1.0 = 0x38), read by the tensor core
+    const uint32_t one = FP8 ? 0x38383838u : 0x3f803f80u;
     for (int st = 0; st < C::kSlots / 2; ++st) {
       uint4* ones = reinterpret_cast<uint4*>(sKV + st * C::kStageBytes + 2 * C::kTileBytes);
-      for (int i = tid; i < C::kOnesBytes / 16; i += C::kThreads) ones[i] = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+      for (int i = tid; i < C::kOnesBytes / 16; i += C::kThreads) ones[i] = make_uint4(one, one, one, one);
     }
     fence_async_shared();
   }
@@ -237,9 +257,14 @@ __global__ void __launch_bounds__(352, 1)
         const uint32_t u = fill / C::kSlots;
         if (!wait_bounded(&bar->kv_empty[s], (u & 1) ^ 1, ctx, kSiteFwdProducer)) return false;
         mbar_arrive_expect_tx(&bar->kv_full[s], C::kTileBytes);
-        const CUtensorMap* map = kv ? &map_v : &map_k;
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_3d(sKV + C::slot_offset(s) + a * 16384, map, &bar->kv_full[s], a * 64, j * 128, bh);
+        if (FP8 && kv) {
+          // V^T of key block j: d rows of 128 keys, tile (bh, j) of the transposed layout
+          tma_load_3d(sKV + C::slot_offset(s), &map_v, &bar->kv_full[s], 0, 0, bh * p.nkb + j);
+        } else {
+          const CUtensorMap* map = kv ? &map_v : &map_k;
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_3d(sKV + C::slot_offset(s) + a * 16384, map, &bar->kv_full[s], a * C::kAtomElems, j * 128, bh);
+        }
         ++fill;
         return true;
       };
@@ -256,14 +281,16 @@ __global__ void __launch_bounds__(352, 1)
         mbar_arrive_expect_tx(&bar->q_full, C::kTileBytes * (has1 ? 2 : 1));
         for (int t = 0; t < (has1 ? 2 : 1); ++t)
           for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &map_q, &bar->q_full, a * 64, w.q0 + 128 * t, w.bh);
+            tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &map_q, &bar->q_full, a * C::kAtomElems, w.q0 + 128 * t,
+                        w.bh);
         ++nq;
         // the next item's queries go to L2 now, so that their load at the
         // item boundary is served from there
         FwdItem nx;
         if (fwd_item<CAUSAL>(p, k + 1, nx) && nx.nb0 > 0)
           for (int t = 0; t < (nx.nb1 > 0 ? 2 : 1); ++t)
-            for (int a = 0; a < C::kAtoms; ++a) tma_prefetch_l2_3d(&map_q, a * 64, nx.q0 + 128 * t, nx.bh);
+            for (int a = 0; a < C::kAtoms; ++a)
+              tma_prefetch_l2_3d(&map_q, a * C::kAtomElems, nx.q0 + 128 * t, nx.bh);
         for (int j = 1; ok && j < nb_max; ++j) ok = load_kv(j, 0, w.bh) && load_kv(j, 1, w.bh);
       }
       // every copy this thread started must land before the CTA can exit
@@ -284,7 +311,7 @@ __global__ void __launch_bounds__(352, 1)
       const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
       const uint64_t qdesc0 = sdesc_sw128(sq, 16, 1024);
       const uint64_t qdesc1 = sdesc_sw128(sq + C::kTileBytes, 16, 1024);
-      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id_s = FP8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
       int s_uses = 0, g = 0, nq = 0;
       bool ok = !(p.debug_stall && !wait_bounded(&bar->never, 0, ctx, kSiteStall));
       FwdItem w;
@@ -311,9 +338,12 @@ __global__ void __launch_bounds__(352, 1)
               tc_fence_after();
               const uint64_t qd = t ? qdesc1 : qdesc0;
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
+              for (int kk = 0; kk < C::kKSteps; ++kk) {
                 const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                mma_bf16_ss(tmem + C::kSCol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
+                if constexpr (FP8)
+                  mma_e4m3_ss(tmem + C::kSCol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
+                else
+                  mma_bf16_ss(tmem + C::kSCol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
               }
               mma_commit(&bar->s_full[t]);
               ++s_uses;
@@ -336,7 +366,8 @@ __global__ void __launch_bounds__(352, 1)
     // V_j is ring fill 2g+1; O_t += P_t(j) V_j once the softmax of tile t wrote P_t(j)
     if (lane == 0) {
       const uint32_t skv = smem_u32(sKV);
-      constexpr uint32_t id_pv = idesc_bf16_f32(128, C::kOCols, false, true);
+      // bf16: V read N-major; FP8: V^T read K-major (with the ones rows after it)
+      constexpr uint32_t id_pv = FP8 ? idesc_e4m3_f32(128, C::kOCols) : idesc_bf16_f32(128, C::kOCols, false, true);
       int g = 0;
       int pv_uses[2] = {0, 0};
       bool ok = true;
@@ -352,7 +383,7 @@ __global__ void __launch_bounds__(352, 1)
             break;
           }
           // (with the row sums, the second 64-column block of B is the ones tile)
-          const uint64_t vdesc = sdesc_sw128(skv + C::slot_offset(vs), 16384, 1024);
+          const uint64_t vdesc = sdesc_sw128(skv + C::slot_offset(vs), FP8 ? 16 : 16384, 1024);
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (j < (t ? w.nb1 : w.nb0)) {
@@ -363,10 +394,18 @@ __global__ void __launch_bounds__(352, 1)
               tc_fence_after();
               const uint32_t dcol = tmem + (t ? C::kOCol1 : C::kOCol0);
               const uint32_t pcol = tmem + (t ? C::kPCol1 : C::kPCol0);
+              if constexpr (FP8) {
+                // 4 steps of 32 keys: P from 8 TMEM columns each, V^T rows at +32 bytes
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 2048) >> 4), id_pv,
-                            (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_e4m3_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 32) >> 4), id_pv,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                  mma_bf16_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 2048) >> 4), id_pv,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+              }
               mma_commit(&bar->pv_done[t]);
               ++pv_uses[t];
             }
@@ -397,9 +436,13 @@ __global__ void __launch_bounds__(352, 1)
       if (nb == 0) continue;
       const int row_q0 = w.q0 + 128 * t;  // first query row of this tile
       const int row_g = row_q0 + r;
+      // FP8: the scores are the E4M3 products times the query and key block scales
+      const float qsl2 = FP8 ? sl2 * __ldg(p.q_scale + (size_t)w.bh * p.nkb + (row_q0 >> 7)) : sl2;
       float m = -CUDART_INF_F;  // exponent reference (log2 units), a stale running max
       float l = 0.f, l_mma = 0.f;
       for (int j = 0; j < nb; ++j, ++uses) {
+        // score factor of this key block (loaded before the wait hides its latency)
+        const float cj = FP8 ? qsl2 * __ldg(p.k_scale + (size_t)w.bh * p.nkb + j) : sl2;
         if (!__all_sync(0xffffffffu, wait_bounded(&bar->s_full[t], uses & 1, ctx, kSiteFwdS))) {
           alive = false;
           break;
@@ -443,7 +486,7 @@ __global__ void __launch_bounds__(352, 1)
           for (int i = 0; i < 5; ++i) t3[i] = max3(t2[3 * i], t2[3 * i + 1], t2[3 * i + 2]);
           mx = max3(max3(t3[0], t3[1], t3[2]), t3[3], t3[4]);
         }
-        const float m_new = fmaxf(m, mx * sl2);
+        const float m_new = fmaxf(m, mx * cj);
         // conditional rescale: move the exponent reference only when the row
         // maximum rose by more than the threshold (always on the first block)
         float alpha = 1.f;
@@ -462,13 +505,15 @@ __global__ void __launch_bounds__(352, 1)
         // probabilities (for the LSE) and `l_mma` of the bf16-rounded ones that
         // the P V product uses (for the normalisation of O, so that the rounding
         // of a dominant probability cancels); four partial sums each.
-        const float2 c2 = make_float2(sl2, sl2);
+        const float2 c2 = make_float2(cj, cj);
         const float2 mneg2 = make_float2(-m, -m);
         float2 acc[4], acc_mma[4];
 #pragma unroll
         for (int a = 0; a < 4; ++a) acc[a] = acc_mma[a] = make_float2(0.f, 0.f);
         // (at d = 64 the sums of the rounded values come from the tensor core)
+        // bf16: two probabilities per 32-bit word; FP8: four (pk[c][0..7] used)
         uint32_t pk[4][16];
+        float hold0 = 0.f, hold1 = 0.f;  // (FP8) the previous pair until its word of four is complete
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -477,7 +522,16 @@ __global__ void __launch_bounds__(352, 1)
                                         c2, mneg2);
             const float p0 = ex2_approx(x.x);
             const float p1 = ex2_approx(x.y);
-            pk[c][i] = pack_bf16x2(p0, p1);
+            if constexpr (FP8) {
+              if (i & 1) {
+                pk[c][i >> 1] = pack_e4m3x4(hold0, hold1, p0, p1);
+              } else {
+                hold0 = p0;
+                hold1 = p1;
+              }
+            } else {
+              pk[c][i] = pack_bf16x2(p0, p1);
+            }
             acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
             if (!C::kSumByMma)
               acc_mma[i & 3] = __fadd2_rn(acc_mma[i & 3], make_float2(__uint_as_float(pk[c][i] << 16),
@@ -522,8 +576,13 @@ __global__ void __launch_bounds__(352, 1)
           }
           tmem_wait_st();
         }
+        if constexpr (FP8) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_st16(tP + 16 * c, pk[c]);
+          for (int c = 0; c < 4; ++c) tmem_st8(tP + 8 * c, pk[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_st16(tP + 16 * c, pk[c]);
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar->p_full[t]);
@@ -554,6 +613,18 @@ __global__ void __launch_bounds__(352, 1)
         tmem_ld32(tO + 32 * c, ov);
         tmem_wait_ld();
         reg_fence32(ov);
+        if constexpr (FP8) {
+          // the value channel scales (the same for every row: broadcast loads)
+          const float4* vs4 = reinterpret_cast<const float4*>(p.v_scale + (size_t)w.bh * D + 32 * c);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 sv = __ldg(vs4 + q4);
+            ov[4 * q4 + 0] = __float_as_uint(__uint_as_float(ov[4 * q4 + 0]) * sv.x);
+            ov[4 * q4 + 1] = __float_as_uint(__uint_as_float(ov[4 * q4 + 1]) * sv.y);
+            ov[4 * q4 + 2] = __float_as_uint(__uint_as_float(ov[4 * q4 + 2]) * sv.z);
+            ov[4 * q4 + 3] = __float_as_uint(__uint_as_float(ov[4 * q4 + 3]) * sv.w);
+          }
+        }
         if (row_g < N) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll

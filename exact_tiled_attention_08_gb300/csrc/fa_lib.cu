@@ -18,6 +18,7 @@
 #include "fa_fwd.cuh"
 #include "fa_bwd.cuh"
 #include "fa_bwd_dq.cuh"
+#include "fa_fp8.cuh"
 
 namespace {
 
@@ -70,6 +71,20 @@ bool encode_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bytes [outer][rows][inner] viewed as a 3-D tensor (inner, rows, outer); boxes of
+// 128 bytes x 128 rows, 128-byte swizzle.  Rows past `rows` read as zero.
+bool encode_u8_3d(CUtensorMap* map, const void* ptr, int inner, int rows, long long outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
+  const cuuint64_t strides[2] = {(cuuint64_t)inner, (cuuint64_t)inner * rows};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // shape checks shared by every entry point
@@ -93,11 +108,11 @@ cudaError_t set_smem(Kernel kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool FP8 = false>
 fa_status launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, fa::FwdParams p,
                      int BH, cudaStream_t stream) {
-  using C = fa::FwdCfg<D>;
-  auto kernel = fa::fa_fwd_kernel<D, CAUSAL>;
+  using C = fa::FwdCfg<D, FP8>;
+  auto kernel = fa::fa_fwd_kernel<D, CAUSAL, FP8>;
   if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
   // persistent CTAs: one per SM (the kernel holds a whole SM), never more than there are items
   int dev = 0, sms = 0;
@@ -176,6 +191,35 @@ struct BwdWorkspace {
     return w;
   }
   size_t total() const { return dq_bytes + 2 * stat_bytes; }
+};
+
+// workspace of fa_fwd_fp8: Q8, K8 [B*H][N][128] E4M3, V8^T [B*H][nkb][128][128]
+// E4M3, query and key block scales [B*H][nkb] fp32, value channel maxima (as
+// bits) and scales [B*H][128] fp32; each part on a 256-byte boundary
+struct Fp8Workspace {
+  size_t q8, k8, v8t, qs, ks, vamax, vs, total;
+  static Fp8Workspace of(int B, int H, int N) {
+    const size_t bh = (size_t)B * H, nkb = (size_t)((N + 127) / 128);
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    Fp8Workspace w;
+    size_t o = 0;
+    w.q8 = o;
+    o += up(bh * N * 128);
+    w.k8 = o;
+    o += up(bh * N * 128);
+    w.v8t = o;
+    o += up(bh * nkb * 128 * 128);
+    w.qs = o;
+    o += up(bh * nkb * 4);
+    w.ks = o;
+    o += up(bh * nkb * 4);
+    w.vamax = o;
+    o += up(bh * 128 * 4);
+    w.vs = o;
+    o += up(bh * 128 * 4);
+    w.total = o;
+    return w;
+  }
 };
 
 // The backward pass proper, given device scratch of BwdWorkspace::total() bytes.
@@ -323,7 +367,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   CUtensorMap mq, mk, mv;
   if (!encode_bhnd(&mq, q, BH, N, d) || !encode_bhnd(&mk, k, BH, N, d) || !encode_bhnd(&mv, v, BH, N, d))
     return FA_ERR_CUDA;
-  fa::FwdParams p;
+  fa::FwdParams p{};
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.N = N;
@@ -334,6 +378,67 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.debug_stall = g_debug_stall.load();
   if (d == 128) return causal ? launch_fwd<128, true>(mq, mk, mv, p, BH, stream) : launch_fwd<128, false>(mq, mk, mv, p, BH, stream);
   return causal ? launch_fwd<64, true>(mq, mk, mv, p, BH, stream) : launch_fwd<64, false>(mq, mk, mv, p, BH, stream);
+}
+
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d) != FA_OK || d != 128) return 0;
+  return Fp8Workspace::of(B, H, N).total;
+}
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, const signed char* signs, void* o, float* lse,
+                     void* workspace, size_t ws_bytes, int B, int H, int N, int d, float scale, int causal,
+                     cudaStream_t stream) {
+  if (!q || !k || !v || !signs || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  fa_status st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if ((st = check_scale(scale, causal)) != FA_OK) return st;
+  if (ws_bytes < fa_fwd_fp8_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
+    return FA_ERR_MISALIGNED;
+  const int BH = B * H;
+  const int nkb = (N + 127) / 128;
+  const Fp8Workspace w = Fp8Workspace::of(B, H, N);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* q8 = ws + w.q8;
+  uint8_t* k8 = ws + w.k8;
+  uint8_t* v8t = ws + w.v8t;
+  float* qs = reinterpret_cast<float*>(ws + w.qs);
+  float* ks = reinterpret_cast<float*>(ws + w.ks);
+  unsigned* vamax = reinterpret_cast<unsigned*>(ws + w.vamax);
+  float* vs = reinterpret_cast<float*>(ws + w.vs);
+  // 1. operands: rotate and quantise Q, K per block; V per channel, transposed
+  const dim3 grid_rows((unsigned)nkb, (unsigned)BH);
+  const auto* qb = static_cast<const __nv_bfloat16*>(q);
+  const auto* kb = static_cast<const __nv_bfloat16*>(k);
+  const auto* vb = static_cast<const __nv_bfloat16*>(v);
+  const int8_t* sg = reinterpret_cast<const int8_t*>(signs);
+  if (cudaMemsetAsync(vamax, 0, (size_t)BH * 128 * sizeof(unsigned), stream) != cudaSuccess) return FA_ERR_CUDA;
+  fa::fa_fp8_rotate_quant_kernel<<<grid_rows, 256, 0, stream>>>(qb, sg, q8, qs, N, nkb);
+  fa::fa_fp8_rotate_quant_kernel<<<grid_rows, 256, 0, stream>>>(kb, sg, k8, ks, N, nkb);
+  fa::fa_fp8_v_amax_kernel<<<grid_rows, 128, 0, stream>>>(vb, vamax, N);
+  fa::fa_fp8_v_quant_kernel<<<grid_rows, 128, 0, stream>>>(vb, vamax, v8t, vs, N, nkb);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  // 2. attention on the E4M3 operands
+  CUtensorMap mq, mk, mv;
+  if (!encode_u8_3d(&mq, q8, 128, N, BH) || !encode_u8_3d(&mk, k8, 128, N, BH) ||
+      !encode_u8_3d(&mv, v8t, 128, 128, (long long)BH * nkb))
+    return FA_ERR_CUDA;
+  fa::FwdParams p{};
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.N = N;
+  p.num_pairs = (N + 255) / 256;
+  p.num_bh = BH;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = wait_limit_ns();
+  p.debug_stall = g_debug_stall.load();
+  p.q_scale = qs;
+  p.k_scale = ks;
+  p.v_scale = vs;
+  p.nkb = nkb;
+  return causal ? launch_fwd<128, true, true>(mq, mk, mv, p, BH, stream)
+                : launch_fwd<128, false, true>(mq, mk, mv, p, BH, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {

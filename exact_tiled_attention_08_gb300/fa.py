@@ -55,6 +55,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
+    lib.fa_fwd_fp8_workspace_bytes.restype = sz
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, vp]
+    lib.fa_fwd_fp8.restype = i
     lib.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp]
     lib.fa_bwd_preprocess.restype = i
     lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
@@ -156,6 +160,29 @@ def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None) -> None:
     _raise(st, "fa_fwd")
 
 
+def fa_fwd_fp8_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().fa_fwd_fp8_workspace_bytes(B, H, N, d))
+
+
+def fa_fwd_fp8(q, k, v, signs, o, lse, workspace, scale: float, causal: bool, stream=None) -> None:
+    """FP8 forward: Q, K rotated by diag(signs) H / sqrt(d) and quantised per
+    128-row block, V per channel, E4M3 products; signs is an int8 device
+    tensor of +1 / -1 [d]; workspace a uint8 device tensor."""
+    B, H, N, d = _shape4(q, "q")
+    dev = q.device
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _check(t, name, torch.bfloat16, (B, H, N, d), dev)
+    _check(lse, "lse", torch.float32, (B, H, N), dev)
+    _check(signs, "signs", torch.int8, (d,), dev)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = load_library().fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), signs.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), workspace.data_ptr(), ws_bytes, B, H, N, d, float(scale),
+                                   int(bool(causal)), _stream_handle(stream))
+    _raise(st, "fa_fwd_fp8")
+
+
 def fa_bwd_preprocess(o, dout, delta, stream=None) -> None:
     """delta = rowsum(dO * O) in fp32, [B,H,N]."""
     B, H, N, d = _shape4(o, "o")
@@ -226,6 +253,16 @@ def attention_forward(q, k, v, scale: float, causal: bool = False, stream=None):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, o, lse, scale, causal, stream)
+    return o, lse
+
+
+def attention_forward_fp8(q, k, v, signs, scale: float, causal: bool = False, workspace=None, stream=None):
+    B, H, N, d = _shape4(q, "q")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(fa_fwd_fp8_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
+    fa_fwd_fp8(q, k, v, signs, o, lse, workspace, scale, causal, stream)
     return o, lse
 
 

@@ -78,6 +78,42 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  float scale, int causal, cudaStream_t stream);
 
 /*
+ * FP8 forward.  "Interrogating the GPU part 5: FlashAttention", section "What
+ * did FlashAttention-3 do with Hopper?" (FP8 quantised per block after a
+ * random Hadamard rotation, which spreads outliers across the block);
+ * "FlashAttention versions", section "FlashAttention-3 (2024)" (block-level
+ * quantisation instead of one per-tensor scale).  Same result as fa_fwd up
+ * to FP8 rounding, with the products on the tensor cores' E4M3 path:
+ *   1. Q and K rows are rotated by R = diag(signs) H / sqrt(128) (H the
+ *      Sylvester Hadamard matrix), which leaves Q K^T unchanged, and rounded
+ *      to E4M3 (nearest even, saturating at +-448) with one scale per block
+ *      of 128 rows of each (batch, head): scale = max|x R| / 448;
+ *   2. V is rounded to E4M3 with one scale per channel of each (batch, head)
+ *      over the sequence: scale = max_n |v_nc| / 448;
+ *   3. the online softmax of fa_fwd runs on the dequantised scores, the
+ *      probabilities are rounded to E4M3 for the P V product, and O is
+ *      normalised by the sum of the rounded probabilities and multiplied by
+ *      the value channel scales.  LSE uses the unrounded sum.
+ *
+ *   q, k, v    in:  bf16 [B][H][N][128]
+ *   signs      in:  int8 [128] device array of +1 / -1 (the random signs of
+ *                   the rotation; the caller draws them)
+ *   o, lse     out: as for fa_fwd
+ *   workspace  device scratch of ws_bytes >= fa_fwd_fp8_workspace_bytes(),
+ *              16-byte aligned.  Layout (each part on a 256-byte boundary,
+ *              in this order): Q R and K R in E4M3 [B][H][N][128];
+ *              V^T in E4M3 [B][H][nkb][128 channels][128 keys] (keys past N
+ *              zero), nkb = ceil(N / 128); query and key block scales fp32
+ *              [B][H][nkb] each; value channel maxima (fp32 bits) and scales
+ *              fp32 [B][H][128] each.  Its contents on entry are ignored.
+ *   d          128 only (other values give FA_ERR_UNSUPPORTED)
+ */
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, const signed char* signs, void* o, float* lse,
+                     void* workspace, size_t ws_bytes, int B, int H, int N, int d, float scale, int causal,
+                     cudaStream_t stream);
+
+/*
  * Backward preprocess: delta_i = sum_c dO_ic * O_ic, one fp32 per query row.
  * The term delta of dS = P o (dP - delta) in "Interrogating the GPU part 5:
  * FlashAttention", section "What does the backward pass do without P?"; the

@@ -22,6 +22,13 @@ Readings taken here (the pages give no formulas):
   scale max|x R| / 448 of the block; values are quantised per channel of one
   head over the whole sequence (scale max_n |v_nc| / 448), so that the scale
   is constant along the P V sum and applies once to the output;
+* a quantised code is a decision that floating point takes, so it is taken
+  in the kernel's precision: the value (x R rounded to fp32, or the bf16 v
+  itself) is multiplied in fp32 by the fp32 reciprocal scale 448 / max, and
+  that fp32 product is rounded to E4M3.  (In fp64 the products that land
+  exactly on an E4M3 midpoint would round differently from fp32 about half
+  of the time when 448 / max is not exact.)  The scales used to dequantise
+  stay fp64;
 * "plain FP8" is one per-tensor scale max|x| / 448 for each of Q, K, V of a
   head, no rotation.
 """
@@ -73,6 +80,15 @@ def _scale_of(amax: np.ndarray) -> np.ndarray:
     return np.where(amax > 0, amax / E4M3_MAX, 1.0)
 
 
+def _codes(x: np.ndarray, amax) -> np.ndarray:
+    """E4M3 codes of x / (max / 448), decided in fp32 (see the module notes):
+    RN(fp32(x) * RN_fp32(448 / max)), then rounded to E4M3."""
+    amax32 = np.asarray(amax, dtype=np.float32)
+    inv = np.where(amax32 > 0, np.float32(E4M3_MAX) / np.where(amax32 > 0, amax32, np.float32(1)), np.float32(1))
+    prod = np.asarray(x, dtype=np.float32) * inv.astype(np.float32)
+    return e4m3_round(prod.astype(np.float64))
+
+
 def quantize_rows_per_block(x, signs=None, block: int = BLOCK):
     """x [N, d] of one head -> (x8 [N, d] E4M3 values, scales [ceil(N/block)]).
 
@@ -88,23 +104,24 @@ def quantize_rows_per_block(x, signs=None, block: int = BLOCK):
     x8 = np.empty_like(xr)
     for b in range(nb):
         rows = slice(b * block, min(n, (b + 1) * block))
-        scales[b] = _scale_of(np.abs(xr[rows]).max())
-        x8[rows] = e4m3_round(xr[rows] / scales[b])
+        amax = np.abs(xr[rows].astype(np.float32)).max()
+        scales[b] = _scale_of(np.float64(amax))
+        x8[rows] = _codes(xr[rows], amax)
     return x8, scales
 
 
 def quantize_columns(x):
     """x [N, d] of one head -> (x8, scales [d]): one scale per channel."""
     x = np.asarray(x, dtype=np.float64)
-    scales = _scale_of(np.abs(x).max(axis=0))
-    return e4m3_round(x / scales[None, :]), scales
+    amax = np.abs(x).max(axis=0)
+    return _codes(x, amax[None, :]), _scale_of(amax)
 
 
 def quantize_per_tensor(x):
     """Plain FP8: one scale for the whole [N, d] operand of one head."""
     x = np.asarray(x, dtype=np.float64)
-    s = float(_scale_of(np.abs(x).max()))
-    return e4m3_round(x / s), s
+    amax = np.abs(x).max()
+    return _codes(x, amax), float(_scale_of(amax))
 
 
 def dequantized_operands(q, k, v, signs):

@@ -123,3 +123,20 @@ def test_binding_checks_tensors_before_calling(lib):
     qb = torch.zeros((1, 1, 8, 128), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fa_fwd(qb, qb, qb, qb, torch.zeros((1, 1, 7)), 0.1, False, stream=0)
+
+
+def test_fwd_fp8_validation(lib):
+    f = lib.fa_fwd_fp8
+    need = lib.fa_fwd_fp8_workspace_bytes(1, 1, 128, 128)
+    assert need > 0 and lib.fa_fwd_fp8_workspace_bytes(1, 1, 128, 64) == 0
+
+    def call(signs=P, ws=P, ws_bytes=need, d=128, scale=0.1, causal=0):
+        return f(VP(P), VP(P), VP(P), VP(signs), VP(P), VP(P), VP(ws), ws_bytes, 1, 1, 128, d, scale, causal, None)
+
+    assert call(signs=0) == fa.FA_ERR_INVALID_ARG
+    assert call(ws=0) == fa.FA_ERR_INVALID_ARG
+    assert call(ws_bytes=need - 1) == fa.FA_ERR_INVALID_ARG
+    assert call(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert call(scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert call(ws=BAD) == fa.FA_ERR_MISALIGNED
+
