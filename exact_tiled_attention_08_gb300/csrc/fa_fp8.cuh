@@ -26,22 +26,73 @@ namespace fa {
 
 constexpr float kE4m3Max = 448.f;
 
-// Q or K: rotate and quantise one 128-row block of one (batch, head) per CTA.
-// 256 threads = 8 warps x 16 rows; a row is 32 lanes x 4 consecutive channels.
-// The rotation is a fast Walsh-Hadamard transform: butterflies (a, b) ->
-// (a + b, a - b) at strides 1 and 2 inside a lane, 4 ... 64 across lanes.
-__global__ void __launch_bounds__(256)
-    fa_fp8_rotate_quant_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict__ signs,
-                               uint8_t* __restrict__ x8, float* __restrict__ scales, int N, int nblk) {
-  constexpr int D = 128, E = 4, kRows = 16;
+// V, pass 1: per-channel maximum of |v| over one key block, folded into
+// amax_bits[bh][c] (non-negative floats order like their bit patterns).
+// 512 threads: thread t reads channels 8 (t % 16) .. +7 of rows t / 16,
+// t / 16 + 32, ... with 16-byte loads (16 threads per 256-byte row), then the
+// 32 row groups are combined through shared memory.
+__device__ __forceinline__ void fp8_v_amax_block(const __nv_bfloat16* __restrict__ v, unsigned* __restrict__ amax_bits,
+                                                 int N, int blk, int bh, float (*part)[128]) {
+  constexpr int D = 128;
+  const int t = threadIdx.x, cg = t & 15, rg = t >> 4;
+  const int rows = min(128, N - blk * 128);
+  const __nv_bfloat16* src = v + ((size_t)bh * N + blk * 128) * D + 8 * cg;
+  float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = rg + 32 * i;
+    if (r < rows) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src + (size_t)r * D));
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h2[e]);
+        m[2 * e] = fmaxf(m[2 * e], fabsf(f.x));
+        m[2 * e + 1] = fmaxf(m[2 * e + 1], fabsf(f.y));
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) part[rg][8 * cg + i] = m[i];
+  __syncthreads();
+  if (t < D) {
+    float mx = part[0][t];
+#pragma unroll
+    for (int g = 1; g < 32; ++g) mx = fmaxf(mx, part[g][t]);
+    atomicMax(amax_bits + (size_t)bh * D + t, __float_as_uint(mx));
+  }
+}
+
+// One launch prepares Q, K (rotation and block quantisation) and the first
+// pass over V (channel maxima), one 128-row block of one (batch, head) per
+// CTA; blockIdx.z selects the operand: 0 = Q, 1 = K, 2 = V.
+//
+// Q or K: 512 threads = 16 warps x 8 rows; a row is 32 lanes x 4 consecutive
+// channels.  The rotation is a fast Walsh-Hadamard transform: butterflies
+// (a, b) -> (a + b, a - b) at strides 1 and 2 inside a lane, 4 ... 64 across
+// lanes.
+__global__ void __launch_bounds__(512)
+    fa_fp8_prepare_kernel(const __nv_bfloat16* __restrict__ x0, const __nv_bfloat16* __restrict__ x1,
+                          const __nv_bfloat16* __restrict__ v, const int8_t* __restrict__ signs,
+                          uint8_t* __restrict__ x8_0, uint8_t* __restrict__ x8_1, float* __restrict__ scales0,
+                          float* __restrict__ scales1, unsigned* __restrict__ v_amax_bits, int N, int nblk) {
+  constexpr int D = 128, E = 4, kRows = 8, kWarps = 16;
+  __shared__ float red[kWarps];
+  __shared__ float part[32][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int blk = blockIdx.x, bh = blockIdx.y;
-  __shared__ float red[8];
+  if (blockIdx.z == 2) {
+    fp8_v_amax_block(v, v_amax_bits, N, blk, bh, part);
+    return;
+  }
+  const __nv_bfloat16* x = blockIdx.z ? x1 : x0;
+  uint8_t* x8 = blockIdx.z ? x8_1 : x8_0;
+  float* scales = blockIdx.z ? scales1 : scales0;
   float sgn[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) sgn[e] = (float)signs[lane * E + e];
   const float inv_sqrt_d = 0.08838834764831845f;  // 1 / sqrt(128)
-  float v[kRows][E];
+  float xr[kRows][E];
   float amax = 0.f;
 #pragma unroll
   for (int r = 0; r < kRows; ++r) {
@@ -74,8 +125,8 @@ __global__ void __launch_bounds__(256)
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      v[r][e] = a[e] * inv_sqrt_d;
-      amax = fmaxf(amax, fabsf(v[r][e]));
+      xr[r][e] = a[e] * inv_sqrt_d;
+      amax = fmaxf(amax, fabsf(xr[r][e]));
     }
   }
 #pragma unroll
@@ -84,7 +135,7 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   amax = red[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+  for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, red[w]);
   const float scale = amax > 0.f ? amax / kE4m3Max : 1.f;
   const float inv = amax > 0.f ? kE4m3Max / amax : 1.f;
 #pragma unroll
@@ -92,54 +143,64 @@ __global__ void __launch_bounds__(256)
     const int row = blk * 128 + warp * kRows + r;
     if (row < N)
       *reinterpret_cast<uint32_t*>(x8 + ((size_t)bh * N + row) * D + lane * E) =
-          pack_e4m3x4(v[r][0] * inv, v[r][1] * inv, v[r][2] * inv, v[r][3] * inv);
+          pack_e4m3x4(xr[r][0] * inv, xr[r][1] * inv, xr[r][2] * inv, xr[r][3] * inv);
   }
   if (threadIdx.x == 0) scales[(size_t)bh * nblk + blk] = scale;
 }
 
-// V, pass 1: per-channel maximum of |v| over one key block, folded into
-// amax_bits[bh][c] (non-negative floats order like their bit patterns).
-// 128 threads, thread = channel.
-__global__ void __launch_bounds__(128)
-    fa_fp8_v_amax_kernel(const __nv_bfloat16* __restrict__ v, unsigned* __restrict__ amax_bits, int N) {
-  constexpr int D = 128;
-  const int c = threadIdx.x, blk = blockIdx.x, bh = blockIdx.y;
-  const int rows = min(128, N - blk * 128);
-  const __nv_bfloat16* src = v + ((size_t)bh * N + blk * 128) * D + c;
-  float m = 0.f;
-  for (int r = 0; r < rows; ++r) m = fmaxf(m, fabsf(__bfloat162float(src[(size_t)r * D])));
-  atomicMax(amax_bits + (size_t)bh * D + c, __float_as_uint(m));
-}
-
-// V, pass 2: quantise one key block per channel and write it transposed:
-// v8t[bh][blk][c][key] (keys past N as zeros); the j = 0 block also writes the
-// channel scales.  128 threads, thread = channel, holding its 128 keys as 32
-// words of four E4M3 values and storing them as one 128-byte row.
-__global__ void __launch_bounds__(128)
+// V, pass 2: quantise one key block per channel and write it transposed,
+// v8t[bh][blk][c][key] (keys past N as zeros); the blk = 0 CTA also writes
+// the channel scales.  256 threads: thread t converts channels 8 (t % 16)
+// .. +7 of four consecutive keys at a time (16-byte loads), packs each
+// channel's four keys into one word of a shared [channel][key / 4] tile, and
+// the tile leaves as 128-byte rows (16-byte stores, consecutive threads on
+// consecutive addresses).
+__global__ void __launch_bounds__(256)
     fa_fp8_v_quant_kernel(const __nv_bfloat16* __restrict__ v, const unsigned* __restrict__ amax_bits,
                           uint8_t* __restrict__ v8t, float* __restrict__ v_scale, int N, int nblk) {
-  constexpr int D = 128;
-  const int c = threadIdx.x, blk = blockIdx.x, bh = blockIdx.y;
-  const float amax = __uint_as_float(amax_bits[(size_t)bh * D + c]);
-  const float inv = amax > 0.f ? kE4m3Max / amax : 1.f;
-  const __nv_bfloat16* src = v + ((size_t)bh * N + blk * 128) * D + c;
-  uint4* dst = reinterpret_cast<uint4*>(v8t + (((size_t)bh * nblk + blk) * D + c) * 128);
-#pragma unroll 1
-  for (int q = 0; q < 8; ++q) {  // 16 keys per 16-byte store
-    uint32_t w[4];
+  constexpr int D = 128, kPad = 33;  // words per tile row: 32 + 1 against bank conflicts
+  __shared__ uint32_t tile[D * kPad];
+  const int t = threadIdx.x, cg = t & 15, kg = t >> 4, blk = blockIdx.x, bh = blockIdx.y;
+  float inv[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float f[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = blk * 128 + 16 * q + 4 * i + e;
-        f[e] = key < N ? __bfloat162float(src[(size_t)(16 * q + 4 * i + e) * D]) * inv : 0.f;
-      }
-      w[i] = pack_e4m3x4(f[0], f[1], f[2], f[3]);
-    }
-    dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+  for (int i = 0; i < 8; ++i) {
+    const float amax = __uint_as_float(amax_bits[(size_t)bh * D + 8 * cg + i]);
+    inv[i] = amax > 0.f ? kE4m3Max / amax : 1.f;
   }
-  if (blk == 0) v_scale[(size_t)bh * D + c] = amax > 0.f ? amax / kE4m3Max : 1.f;
+  const __nv_bfloat16* src = v + ((size_t)bh * N + blk * 128) * D + 8 * cg;
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int kw = kg + 16 * it;  // word of four keys 4 kw .. 4 kw + 3
+    float f[4][8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int key = blk * 128 + 4 * kw + e;
+      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+      if (key < N) raw = __ldg(reinterpret_cast<const uint4*>(src + (size_t)(4 * kw + e) * D));
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 x = __bfloat1622float2(h2[i]);
+        f[e][2 * i] = x.x * inv[2 * i];
+        f[e][2 * i + 1] = x.y * inv[2 * i + 1];
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tile[(8 * cg + i) * kPad + kw] = pack_e4m3x4(f[0][i], f[1][i], f[2][i], f[3][i]);
+  }
+  __syncthreads();
+  uint8_t* dst = v8t + ((size_t)bh * nblk + blk) * D * 128;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int id = t + 256 * i;  // 16-byte chunk id: row id / 8, chunk id % 8
+    const int c = id >> 3, q = id & 7;
+    const uint32_t* w = tile + c * kPad + 4 * q;
+    *reinterpret_cast<uint4*>(dst + (size_t)c * 128 + 16 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (blk == 0 && t < D) {
+    const float amax = __uint_as_float(amax_bits[(size_t)bh * D + t]);
+    v_scale[(size_t)bh * D + t] = amax > 0.f ? amax / kE4m3Max : 1.f;
+  }
 }
 
 }  // namespace fa

@@ -414,10 +414,9 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, const signed c
   const auto* vb = static_cast<const __nv_bfloat16*>(v);
   const int8_t* sg = reinterpret_cast<const int8_t*>(signs);
   if (cudaMemsetAsync(vamax, 0, (size_t)BH * 128 * sizeof(unsigned), stream) != cudaSuccess) return FA_ERR_CUDA;
-  fa::fa_fp8_rotate_quant_kernel<<<grid_rows, 256, 0, stream>>>(qb, sg, q8, qs, N, nkb);
-  fa::fa_fp8_rotate_quant_kernel<<<grid_rows, 256, 0, stream>>>(kb, sg, k8, ks, N, nkb);
-  fa::fa_fp8_v_amax_kernel<<<grid_rows, 128, 0, stream>>>(vb, vamax, N);
-  fa::fa_fp8_v_quant_kernel<<<grid_rows, 128, 0, stream>>>(vb, vamax, v8t, vs, N, nkb);
+  fa::fa_fp8_prepare_kernel<<<dim3((unsigned)nkb, (unsigned)BH, 3), 512, 0, stream>>>(qb, kb, vb, sg, q8, k8, qs, ks,
+                                                                                  vamax, N, nkb);
+  fa::fa_fp8_v_quant_kernel<<<grid_rows, 256, 0, stream>>>(vb, vamax, v8t, vs, N, nkb);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   // 2. attention on the E4M3 operands
   CUtensorMap mq, mk, mv;
