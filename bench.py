@@ -340,6 +340,39 @@ def run_ours(args, rank, world, local):
         st = fa.fa_check_device_status(stream)
         if st != fa.FA_OK:
             raise SystemExit(f"bench.py: device status {fa.fa_status_string(st)} in the timed region")
+    # ---- the FP8 forward (fa_fwd_fp8) on the same inputs, d = 128 only: the
+    # whole call (operand preparation + E4M3 attention kernel) and the kernel
+    fp8 = None
+    if w.d == 128:
+        signs = torch.ones(w.d, dtype=torch.int8, device=dev)
+        ws8 = torch.empty(fa.fa_fwd_fp8_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+        o8 = torch.empty_like(o)
+        lse8 = torch.empty_like(lse)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fa.fa_fwd_fp8(q, k, v, signs, o8, lse8, ws8, scale, w.causal, stream)
+            calls, kers = [], []
+            for _ in range(20):
+                flush.zero_()
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                for x in e:
+                    x.record(stream)
+                fa.fa_set_timing_events(e[2], e[3], None, None)
+                e[0].record(stream)
+                fa.fa_fwd_fp8(q, k, v, signs, o8, lse8, ws8, scale, w.causal, stream)
+                e[1].record(stream)
+                calls.append(e)
+            torch.cuda.synchronize(dev)
+            fa.fa_set_timing_events()
+            if fa.fa_check_device_status(stream) != fa.FA_OK:
+                raise SystemExit("bench.py: device status error in the FP8 forward")
+        call_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in calls)
+        ker_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in calls)
+        fp8 = {"call_ms": call_ms, "call_tflops": fwd_flops / (call_ms / 1e3) / 1e12, "kernel_ms": ker_ms,
+               "kernel_tflops": fwd_flops / (ker_ms / 1e3) / 1e12,
+               "note": "fa_fwd_fp8: Q, K rotated and quantised per 128-row block, V per channel, E4M3 products; "
+                       "the call includes the operand preparation"}
+
     step_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     fwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
     bwd_ms = statistics.mean(e[4].elapsed_time(e[5]) for e in ev)
@@ -457,7 +490,8 @@ def run_ours(args, rank, world, local):
         "roofline": roofline,
         "breakdown": {"fwd_kernel_ms": fwd_ms, "fwd_tflops": fwd_tf, "bwd_kernel_ms": bwd_ms, "bwd_tflops": bwd_tf,
                       "other_ms": step_ms - fwd_ms - bwd_ms,
-                      "fwd_frac_of_sustained_peak": fwd_tf / peak, "bwd_frac_of_sustained_peak": bwd_tf / peak},
+                      "fwd_frac_of_sustained_peak": fwd_tf / peak, "bwd_frac_of_sustained_peak": bwd_tf / peak,
+                      "fp8_forward": fp8},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "chunks": chunks, "steps": E,
                 "pipelining": "head chunks over copy-in/compute/copy-out streams; device buffers double-buffered "
