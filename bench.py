@@ -42,7 +42,7 @@ DEFAULT_WORKLOAD = "b4_h16_n2048_d128"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = ["fa_fwd.cuh", "fa_bwd.cuh", "fa_bwd_dq.cuh", "sm103_ptx.cuh", "fa_lib.cu"]
+KERNEL_SOURCES = ["fa_fwd.cuh", "fa_bwd.cuh", "fa_bwd_dq.cuh", "fa_fp8.cuh", "sm103_ptx.cuh", "fa_lib.cu"]
 
 
 def parse_args():
