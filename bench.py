@@ -42,7 +42,15 @@ DEFAULT_WORKLOAD = "b4_h16_n2048_d128"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = ["fa_fwd.cuh", "fa_bwd.cuh", "fa_bwd_dq.cuh", "fa_fp8.cuh", "sm103_ptx.cuh", "fa_lib.cu"]
+# the sources each kernel's DRAM traffic depends on (its own header, the PTX
+# building blocks and the host code that configures its launch)
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ["fa_fwd.cuh", "sm103_ptx.cuh", "fa_lib.cu"],
+    "fa_fwd_kernel/fp8": ["fa_fwd.cuh", "fa_fp8.cuh", "sm103_ptx.cuh", "fa_lib.cu"],
+    "fa_bwd_kernel": ["fa_bwd.cuh", "sm103_ptx.cuh", "fa_lib.cu"],
+    "fa_bwd_kernel/deterministic": ["fa_bwd.cuh", "sm103_ptx.cuh", "fa_lib.cu"],
+    "fa_bwd_dq_kernel": ["fa_bwd_dq.cuh", "sm103_ptx.cuh", "fa_lib.cu"],
+}
 
 
 def parse_args():
@@ -106,9 +114,9 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str = "fa_bwd_kernel") -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "exact_tiled_attention_08_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -122,7 +130,7 @@ def recorded_traffic(kernel: str, workload: str):
     with open(TRAFFIC_FILE) as f:
         d = json.load(f)
     e = d.get(kernel, {}).get(workload)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or kernel not in KERNEL_SOURCES or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 

@@ -71,20 +71,22 @@ struct FwdCfg {
   static constexpr int kKSteps = D * kElemBytes / 32;             // MMAs of the S product (32 bytes of K each)
   static constexpr int kThreads = 352;
   static constexpr uint32_t kTmemCols = 512;
-  // At d = 64 (and in FP8) the tensor core also forms the row sums of the
-  // rounded P that the output product uses: each V operand in the ring is
-  // followed by ones, the product O += P [V | 1] is 16 columns wider, and
-  // those columns hold sum_k P_rk, rescaled together with O.  bf16 d = 64:
-  // V is read N-major and the ones are a 64-column atom of bf16 ones after it;
-  // FP8: V^T is read K-major and the ones are 16 more rows of E4M3 ones.  At
-  // bf16 d = 128 the columns are not there (S 128 + P 2 x 64 + O 2 x 128 =
-  // 512) and the softmax sums the rounded values itself.
-  static constexpr bool kSumByMma = FP8 || (D == 64);
+  // In FP8 the tensor core also forms the row sums of the rounded P that the
+  // output product uses: V^T (read K-major) is followed by 16 rows of E4M3
+  // ones, the product O += P [V | 1] is 16 columns wider, and those columns
+  // hold sum_k P_rk, rescaled together with O.  In bf16 the softmax sums the
+  // rounded values itself.
+  static constexpr bool kSumByMma = FP8;
   static constexpr int kOCols = kSumByMma ? D + 16 : D;  // O accumulator columns
-  static constexpr int kOnesBytes = FP8 ? 16 * 128 : (kSumByMma ? 16384 : 0);
+  static constexpr int kOnesBytes = FP8 ? 16 * 128 : 0;
+  // bf16 d = 64: a score buffer per tile (S_0 first, S_1 after the O
+  // accumulators: 128 + 2 x 64 + 2 x 64 + 128 = 512 columns), so that a tile's
+  // next scores never wait for the other tile to load its own.  At d = 128
+  // (and in FP8) the two tiles share one buffer and take turns on it.
+  static constexpr bool kDualS = !FP8 && (D == 64);
   // K_j is ring fill 2j, V_j fill 2j+1; with the ones tiles the slots come in
   // pairs (K, V, ones), so the slot count is even
-  static constexpr int kSlots = FP8 ? 10 : ((D == 128) ? 5 : 8);
+  static constexpr int kSlots = FP8 ? 10 : ((D == 128) ? 5 : 12);
   static_assert(!kSumByMma || kSlots % 2 == 0, "K/V slot pairs");
   static constexpr int kStageBytes = 2 * kTileBytes + kOnesBytes;
   static constexpr int kRingBytes = kSumByMma ? (kSlots / 2) * kStageBytes : kSlots * kTileBytes;
@@ -95,6 +97,8 @@ struct FwdCfg {
   static constexpr uint32_t kPCols = FP8 ? 32 : 64;
   static constexpr uint32_t kSCol = 0, kPCol0 = 128, kPCol1 = 128 + kPCols;
   static constexpr uint32_t kOCol0 = 128 + 2 * kPCols, kOCol1 = kOCol0 + kOCols;
+  static constexpr uint32_t kSCol1 = kDualS ? kOCol1 + kOCols : kSCol;  // tile 1's score buffer
+  static_assert(!kDualS || kSCol1 + 128 <= kTmemCols, "tensor memory budget");
   static_assert(kOCol1 + kOCols <= kTmemCols, "tensor memory budget");
   static constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kRingBytes + 512;
 };
@@ -105,7 +109,8 @@ struct FwdBarriers {
   uint64_t kv_full[16];
   uint64_t kv_empty[16];
   uint64_t s_full[2];   // S holds tile t's scores (MMA commit)
-  uint64_t s_free;      // the tile that used S last has loaded it (128 softmax threads)
+  uint64_t s_free[2];   // the tile that used a score buffer last has loaded it (128 softmax threads;
+                        // one buffer, index 0, unless each tile has its own)
   uint64_t p_full[2];   // P_t written, O_t corrected (128 softmax threads)
   uint64_t pv_done[2];  // O_t += P_t V complete (MMA commit)
   uint64_t drain[2];    // one per issuing thread
@@ -221,7 +226,8 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(&bar->p_full[t], 128);
       mbar_init(&bar->pv_done[t], 1);
     }
-    mbar_init(&bar->s_free, 128);
+    mbar_init(&bar->s_free[0], 128);
+    mbar_init(&bar->s_free[1], 128);
     mbar_init(&bar->drain[0], 1);
     mbar_init(&bar->drain[1], 1);
     mbar_init(&bar->never, 1);
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(352, 1)
       const uint64_t qdesc0 = sdesc_sw128(sq, 16, 1024);
       const uint64_t qdesc1 = sdesc_sw128(sq + C::kTileBytes, 16, 1024);
       constexpr uint32_t id_s = FP8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
-      int s_uses = 0, g = 0, nq = 0;
+      int s_uses[2] = {0, 0}, g = 0, nq = 0;  // S products issued into each score buffer
       bool ok = !(p.debug_stall && !wait_bounded(&bar->never, 0, ctx, kSiteStall));
       FwdItem w;
       for (int k = 0; ok && fwd_item<CAUSAL>(p, k, w); ++k) {
@@ -331,7 +337,8 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (j < (t ? w.nb1 : w.nb0)) {
-              if (s_uses > 0 && !wait_bounded(&bar->s_free, (s_uses - 1) & 1, ctx, kSiteFwdSFree)) {
+              const int sb = C::kDualS ? t : 0;
+              if (s_uses[sb] > 0 && !wait_bounded(&bar->s_free[sb], (s_uses[sb] - 1) & 1, ctx, kSiteFwdSFree)) {
                 ok = false;
                 break;
               }
@@ -340,13 +347,14 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
               for (int kk = 0; kk < C::kKSteps; ++kk) {
                 const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                const uint32_t scol = tmem + (sb ? C::kSCol1 : C::kSCol);
                 if constexpr (FP8)
-                  mma_e4m3_ss(tmem + C::kSCol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
+                  mma_e4m3_ss(scol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
                 else
-                  mma_bf16_ss(tmem + C::kSCol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
+                  mma_bf16_ss(scol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
               }
               mma_commit(&bar->s_full[t]);
-              ++s_uses;
+              ++s_uses[sb];
             }
           }
           if (!ok) break;
@@ -424,7 +432,7 @@ __global__ void __launch_bounds__(352, 1)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + C::kSCol + lane_off;
+    const uint32_t tS = tmem + ((C::kDualS && t) ? C::kSCol1 : C::kSCol) + lane_off;
     const uint32_t tP = tmem + (t ? C::kPCol1 : C::kPCol0) + lane_off;
     const uint32_t tO = tmem + (t ? C::kOCol1 : C::kOCol0) + lane_off;
     const float sl2 = p.scale_log2;
@@ -454,9 +462,9 @@ __global__ void __launch_bounds__(352, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
-        // the scores are in registers: the other tile's scores may now overwrite S
+        // the scores are in registers: the next scores may now overwrite S
         tc_fence_before();
-        mbar_arrive(&bar->s_free);
+        mbar_arrive(&bar->s_free[C::kDualS ? t : 0]);
 
         const int kbase = j * 128;
         const bool tail = kbase + 128 > N;
