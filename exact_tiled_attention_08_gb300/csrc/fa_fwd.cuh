@@ -206,8 +206,8 @@ __global__ void __launch_bounds__(352, 1)
   const int N = p.N;
 
   if (C::kSumByMma) {
-    // the ones after each V slot (bf16 1.0 = 0x3f80, E4M3 1.0 = 0x38), read by the tensor core
-    const uint32_t one = FP8 ? 0x38383838u : 0x3f803f80u;
+    // (FP8) the E4M3 ones (0x38) after each V^T slot, read by the tensor core
+    const uint32_t one = 0x38383838u;
     for (int st = 0; st < C::kSlots / 2; ++st) {
       uint4* ones = reinterpret_cast<uint4*>(sKV + st * C::kStageBytes + 2 * C::kTileBytes);
       for (int i = tid; i < C::kOnesBytes / 16; i += C::kThreads) ones[i] = make_uint4(one, one, one, one);
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(352, 1)
             ok = false;
             break;
           }
-          // (with the row sums, the second 64-column block of B is the ones tile)
+          // (FP8: the ones rows after V^T make the last 16 columns of O the row sums)
           const uint64_t vdesc = sdesc_sw128(skv + C::slot_offset(vs), FP8 ? 16 : 16384, 1024);
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
