@@ -24,9 +24,11 @@
 // between groups of MMAs leaves the tensor core idle, so the two kinds of
 // product are issued by two threads whose waits overlap each other's MMAs.
 // Tensor memory (512 columns): one score buffer S (128 fp32 columns) that the
-// two tiles use in turn, the bf16 probabilities P_0, P_1 (64 columns each)
-// and the output accumulators O_0, O_1 (d columns each).  Shared memory: Q_0,
-// Q_1 and a ring of K/V tiles, all with 128-byte swizzle.
+// two tiles use in turn (at d = 64 one per tile), the bf16 probabilities
+// P_0, P_1 (64 columns each) and the output accumulators O_0, O_1 (d columns
+// each).  Shared memory: Q_0, Q_1 and a ring of K/V tiles, all with 128-byte
+// swizzle.  The FP8 instance (FwdCfg<D, true>) keeps this structure with
+// E4M3 operands; its differences are described at FwdCfg.
 //
 // Per key block j the tiles alternate on S: S_0(j), S_1(j), S_0(j+1), ...; a
 // softmax releases S as soon as it has loaded its scores into registers, so

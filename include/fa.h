@@ -233,11 +233,13 @@ void fa_set_wait_limit_ns(unsigned long long limit_ns);
 void fa_debug_stall(int enable);
 
 /*
- * Profiling hook.  While set, fa_fwd records fwd_start and fwd_stop on its
- * stream immediately before and after launching its attention kernel, and
- * fa_bwd records bwd_start and bwd_stop around its main backward kernel (not
- * around the preprocess or the final dQ cast), so that cudaEventElapsedTime
- * gives the duration of exactly those kernels.  The events are created and
+ * Profiling hook.  While set, fa_fwd and fa_fwd_fp8 record fwd_start and
+ * fwd_stop on their stream immediately before and after launching the
+ * attention kernel (not around fa_fwd_fp8's operand preparation), and fa_bwd
+ * and fa_bwd_deterministic record bwd_start and bwd_stop around the main
+ * backward kernel (not around the preprocess, the final dQ cast or the
+ * deterministic dQ pass), so that cudaEventElapsedTime gives the duration of
+ * exactly those kernels.  The events are created and
  * owned by the caller on the device the calls run on; a null pointer disables
  * its pair.  Process-wide; call again with nulls to turn it off.
  */
