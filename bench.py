@@ -22,6 +22,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -114,11 +115,19 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace runs collapsed, so that
+    editing a comment does not count as changing a kernel."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel: str = "fa_bwd_kernel") -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "exact_tiled_attention_08_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "exact_tiled_attention_08_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

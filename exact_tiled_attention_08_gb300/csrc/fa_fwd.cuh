@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(352, 1)
         float2 acc[4], acc_mma[4];
 #pragma unroll
         for (int a = 0; a < 4; ++a) acc[a] = acc_mma[a] = make_float2(0.f, 0.f);
-        // (at d = 64 the sums of the rounded values come from the tensor core)
+        // (in FP8 the sums of the rounded values come from the tensor core)
         // bf16: two probabilities per 32-bit word; FP8: four (pk[c][0..7] used)
         uint32_t pk[4][16];
         float hold0 = 0.f, hold1 = 0.f;  // (FP8) the previous pair until its word of four is complete
@@ -598,7 +598,7 @@ __global__ void __launch_bounds__(352, 1)
         mbar_arrive(&bar->p_full[t]);
       }
       if (!alive) break;
-      // epilogue: O = o / l_mma (at d = 64 from the extra O columns), LSE = (m + log2 l) ln 2.
+      // epilogue: O = o / l_mma (in FP8 from the extra O columns), LSE = (m + log2 l) ln 2.
       // Once the tensor memory loads below have completed, the next item's
       // first P V product may overwrite O_t (it is issued only after this
       // warpgroup has written the next P_t).
