@@ -112,7 +112,16 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------------------
-// main backward kernel: one CTA per (key block j, batch, head).
+// main backward kernel: the work is one item per (key block j, batch, head).
+// With the causal mask one CTA runs per item (the items' costs range from 1
+// to nkb query blocks, and the hardware's CTA scheduler balances them);
+// without it the CTAs are persistent, one per SM, and walk the items
+// blockIdx.x, blockIdx.x + gridDim.x, ...  All pipeline counters (ring
+// fills, per-block barrier phases, statistics entries) run on across the
+// items, so a CTA loads the next item's first Q tile while the current item
+// finishes, its K and V as soon as the last dK and dQ products have read the
+// old ones, and the reducers' last dQ_i and the dK, dV write-out overlap with
+// the next item's first products.
 //
 // K_j and V_j (128 keys) stay in shared memory; the query blocks i (all of
 // them, or i >= j when causal) stream Q_i (with its rows' LSE log2(e) and
@@ -137,7 +146,7 @@ __global__ void __launch_bounds__(256)
 // elementwise warps never wait for it.
 //
 // Warp roles (512 threads, four warpgroups; register budgets set with
-// setmaxnreg, 144 + 144 + 144 + 80 per thread = the launch's 128 x 4):
+// setmaxnreg, 144 + 144 + 152 + 72 per thread = the launch's 128 x 4):
 //   warps 0-7   elementwise: warpgroup g owns query columns [64 g, 64 g + 64)
 //               of dS
 //   warps 8-11  reducers: warp 8 + q takes TMEM lanes 32q.. (query rows) of
@@ -154,13 +163,15 @@ __global__ void __launch_bounds__(256)
 // of that group's own S^T columns, which only the writing thread has read;
 // dQ_i goes into the dP^T columns once the elementwise step has read them.
 // ---------------------------------------------------------------------------
-// Register budgets per thread after setmaxnreg: the elementwise and reducer
-// warpgroups take kBwdWorkRegs, the issuing/producer warpgroup keeps
-// kBwdMiscRegs.  Each SM sub-partition holds one warp of every warpgroup, so
-// 3 x 144 + 80 = 512 = 4 x 128 uses exactly the registers the block was
-// launched with (128 per thread, which the host checks before launching).
-constexpr uint32_t kBwdWorkRegs = 144, kBwdMiscRegs = 80;
-static_assert(3 * kBwdWorkRegs + kBwdMiscRegs == 4 * 128, "register split must match the launch budget");
+// Register budgets per thread after setmaxnreg: the two elementwise
+// warpgroups take kBwdWorkRegs, the reducers kBwdRedRegs (a reducer holds its
+// 32 rows of dQ_i, D values each, in registers), the issuing/producer
+// warpgroup keeps kBwdMiscRegs.  Each SM sub-partition holds one warp of
+// every warpgroup, so 2 x 144 + 152 + 72 = 512 = 4 x 128 uses exactly the
+// registers the block was launched with (128 per thread, which the host
+// checks before launching).
+constexpr uint32_t kBwdWorkRegs = 144, kBwdRedRegs = 152, kBwdMiscRegs = 72;
+static_assert(2 * kBwdWorkRegs + kBwdRedRegs + kBwdMiscRegs == 4 * 128, "register split must match the launch budget");
 
 // kAtomicDq: the kernel also forms dQ_i = dS K_j and adds it into the fp32
 // accumulator (reducer warps); otherwise dQ is left to the separate
@@ -209,11 +220,45 @@ struct BwdParams {
   __nv_bfloat16* dv_out;
   int N;
   int nkb;           // key (and query) blocks per head
+  int num_items;     // (key block, batch, head) items: nkb * batch * heads
+  int num_bh;        // batch * heads
+  int group_heads;   // with the mask: heads per group of the item order (see bwd_item)
   float scale_log2;  // scale * log2(e)
   float scale;
   uint64_t wait_limit_ns;
   int debug_stall;  // nonzero: issuer A first waits on `never` (tests the timeout path)
 };
+
+// The CTA's items: blockIdx.x, blockIdx.x + gridDim.x, ...
+// Without the mask item k is key block k % nkb of (batch, head) k / nkb, so
+// that the CTAs running at one time work on few heads, whose Q and dO tiles
+// they share through L2.  With the mask item j costs nkb - j query blocks;
+// the items go in groups of group_heads heads, and inside a group by key
+// block first (j = 0, the costliest, for every head of the group, then
+// j = 1, ...): the hardware hands the costliest items out first, so that the
+// last SMs to finish end on one-block items, while a group's Q and dO still
+// fit in L2.
+struct BwdItem {
+  int bh, jb, i_start, n_it;
+};
+template <bool CAUSAL>
+__device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int k) {
+  BwdItem t;
+  if (CAUSAL) {
+    const int per_group = p.group_heads * p.nkb;
+    const int grp = k / per_group;
+    const int r = k - grp * per_group;
+    const int gh = min(p.group_heads, p.num_bh - grp * p.group_heads);  // heads in this group
+    t.jb = r / gh;
+    t.bh = grp * p.group_heads + (r - t.jb * gh);
+  } else {
+    t.bh = k / p.nkb;
+    t.jb = k - t.bh * p.nkb;
+  }
+  t.i_start = CAUSAL ? t.jb : 0;
+  t.n_it = p.nkb - t.i_start;
+  return t;
+}
 
 enum : int { kSiteBwdProducer = 16, kSiteBwdKV, kSiteBwdQ, kSiteBwdDo, kSiteBwdDvDone, kSiteBwdDqFree, kSiteBwdEw,
              kSiteBwdS, kSiteBwdDp, kSiteBwdDq, kSiteBwdAcc };
@@ -243,11 +288,6 @@ __global__ void __launch_bounds__(512, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N;
-  const int jb = blockIdx.x % p.nkb;
-  const int bh = blockIdx.x / p.nkb;
-  const int k0 = jb * 128;
-  const int i_start = CAUSAL ? jb : 0;
-  const int n_it = p.nkb - i_start;
 
   if (tid == 0) {
     mbar_init(&bar->kv_full, 1);
@@ -291,18 +331,31 @@ __global__ void __launch_bounds__(512, 1)
     setmaxnreg_dec<kBwdMiscRegs>();
     if (warp == 13) {
       // ---------------------------------------------------------------- TMA producer
-      // ring fills: Q_i (with its LSE*log2e and delta rows) at 2 it, dO_i at 2 it + 1
+      // ring fills, counted over all of the CTA's items: the g-th query
+      // block's Q_i (with its LSE*log2e and delta rows) at 2 g, dO_i at
+      // 2 g + 1.
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bar->kv_full, 2 * C::kTileBytes);
-        for (int a = 0; a < C::kAtoms; ++a) {
-          tma_load_3d(sK + a * 16384, &map_k, &bar->kv_full, a * 64, k0, bh);
-          tma_load_3d(sV + a * 16384, &map_v, &bar->kv_full, a * 64, k0, bh);
-        }
-        int fill = 0;
+        int fill = 0, g = 0, w = 0, kv_loads = 0;
         bool ok = true;
-        for (int it = 0; ok && it < n_it; ++it) {
-          const int i = i_start + it;
+        for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x, ++w) {
+         const BwdItem t = bwd_item<CAUSAL>(p, item);
+         for (int it = 0; ok && it < t.n_it; ++it, ++g) {
+          const int i = t.i_start + it;
           for (int which = 0; which < 2; ++which) {
+            // K and V of the item go first, once the previous item's last
+            // products (acc_done) have read the old ones
+            if (!which && it == 0) {
+              if (w > 0 && !wait_bounded_inl(&bar->acc_done, (w - 1) & 1, ctx, kSiteBwdProducer)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&bar->kv_full, 2 * C::kTileBytes);
+              for (int a = 0; a < C::kAtoms; ++a) {
+                tma_load_3d(sK + a * 16384, &map_k, &bar->kv_full, a * 64, t.jb * 128, t.bh);
+                tma_load_3d(sV + a * 16384, &map_v, &bar->kv_full, a * 64, t.jb * 128, t.bh);
+              }
+              ++kv_loads;
+            }
             const int s = fill % C::kSlots;
             const uint32_t u = fill / C::kSlots;
             if (!wait_bounded_inl(&bar->ring_empty[s], (u & 1) ^ 1, ctx, kSiteBwdProducer)) {
@@ -312,23 +365,24 @@ __global__ void __launch_bounds__(512, 1)
             mbar_arrive_expect_tx(&bar->ring_full[s], C::kTileBytes + (which ? 0 : C::kStatBytes));
             const CUtensorMap* map = which ? &map_do : &map_q;
             for (int a = 0; a < C::kAtoms; ++a)
-              tma_load_3d(sRing + s * C::kTileBytes + a * 16384, map, &bar->ring_full[s], a * 64, i * 128, bh);
+              tma_load_3d(sRing + s * C::kTileBytes + a * 16384, map, &bar->ring_full[s], a * 64, i * 128, t.bh);
             // with a three-slot ring the same tile of the next query block goes
             // to L2 now, so that its load (which waits for a free slot) is
             // served from L2
-            if (C::kSlots < 4 && it + 1 < n_it)
-              for (int a = 0; a < C::kAtoms; ++a) tma_prefetch_l2_3d(map, a * 64, (i + 1) * 128, bh);
+            if (C::kSlots < 4 && it + 1 < t.n_it)
+              for (int a = 0; a < C::kAtoms; ++a) tma_prefetch_l2_3d(map, a * 64, (i + 1) * 128, t.bh);
             if (!which) {
               // the entry was last read by the elementwise step of block
-              // it - kStatEntries, which has finished once this slot is free
-              uint8_t* st = sStat + (it % C::kStatEntries) * C::kStatBytes;
-              tma_load_2d(st, &map_lse2, &bar->ring_full[s], i * 128, bh);
-              tma_load_2d(st + 512, &map_delta, &bar->ring_full[s], i * 128, bh);
+              // g - kStatEntries, which has finished once this slot is free
+              uint8_t* st = sStat + (g % C::kStatEntries) * C::kStatBytes;
+              tma_load_2d(st, &map_lse2, &bar->ring_full[s], i * 128, t.bh);
+              tma_load_2d(st + 512, &map_delta, &bar->ring_full[s], i * 128, t.bh);
             }
             ++fill;
           }
+         }
         }
-        wait_drain_inl(&bar->kv_full, 0, kDrainLimitNs);
+        if (kv_loads > 0) wait_drain_inl(&bar->kv_full, (kv_loads - 1) & 1, kDrainLimitNs);
         for (int s = 0; s < C::kSlots; ++s) {
           if (fill > s) {
             const int uses = (fill - 1 - s) / C::kSlots + 1;
@@ -346,19 +400,23 @@ __global__ void __launch_bounds__(512, 1)
         const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16, 1024);
         const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDpCol;
         bool ok = !(p.debug_stall && !wait_bounded_inl(&bar->never, 0, ctx, kSiteStall));
-        ok = ok && wait_bounded_inl(&bar->kv_full, 0, ctx, kSiteBwdKV);
         // S^T goes first: the first half of the elementwise step needs only
         // S^T, its columns are free as soon as dV of the previous block has
         // run, and (with a three-slot ring) dO_i may still be on its way.
-        for (int it = 0; ok && it < n_it; ++it) {
+        // g counts query blocks over all of the CTA's items, w the items.
+        int g = 0, w = 0;
+        for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x, ++w) {
+         const BwdItem t = bwd_item<CAUSAL>(p, item);
+         ok = wait_bounded_inl(&bar->kv_full, w & 1, ctx, kSiteBwdKV);
+         for (int it = 0; ok && it < t.n_it; ++it, ++g) {
 #pragma unroll
           for (int step = 0; step < 2; ++step) {
             if (step == 0) {
               // S^T = K Q_i^T, once dV has consumed the previous P^T held in
               // these columns
-              const int fq = 2 * it, sq = fq % C::kSlots;
+              const int fq = 2 * g, sq = fq % C::kSlots;
               if (!wait_bounded_inl(&bar->ring_full[sq], (fq / C::kSlots) & 1, ctx, kSiteBwdQ)) { ok = false; break; }
-              if (it > 0 && !wait_bounded_inl(&bar->dv_done, (it - 1) & 1, ctx, kSiteBwdDvDone)) { ok = false; break; }
+              if (g > 0 && !wait_bounded_inl(&bar->dv_done, (g - 1) & 1, ctx, kSiteBwdDvDone)) { ok = false; break; }
               tc_fence_after();
               const uint64_t qdesc = sdesc_sw128(ring + sq * C::kTileBytes, 16, 1024);
 #pragma unroll
@@ -371,10 +429,10 @@ __global__ void __launch_bounds__(512, 1)
               // dP^T = V dO_i^T, once the reducers have taken the previous dQ
               // out of these columns (without dQ: once the elementwise step
               // has read the previous dP^T)
-              const int fd = 2 * it + 1, sd = fd % C::kSlots;
+              const int fd = 2 * g + 1, sd = fd % C::kSlots;
               if (!wait_bounded_inl(&bar->ring_full[sd], (fd / C::kSlots) & 1, ctx, kSiteBwdDo)) { ok = false; break; }
-              if (it > 0 && !wait_bounded_inl(kAtomicDq ? &bar->dq_free : &bar->ew_done, (it - 1) & 1, ctx,
-                                              kSiteBwdDqFree)) {
+              if (g > 0 && !wait_bounded_inl(kAtomicDq ? &bar->dq_free : &bar->ew_done, (g - 1) & 1, ctx,
+                                             kSiteBwdDqFree)) {
                 ok = false;
                 break;
               }
@@ -388,6 +446,7 @@ __global__ void __launch_bounds__(512, 1)
               mma_commit(&bar->dp_full);
             }
           }
+         }
         }
         mma_commit(&bar->drain[0]);
         wait_drain_inl(&bar->drain[0], 0, kDrainLimitNs);
@@ -405,15 +464,19 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDpCol;
         const uint32_t tDK = tmem + C::kDkCol, tDV = tmem + C::kDvCol;
         bool ok = true;
-        for (int it = 0; ok && it < n_it; ++it) {
-          const int sq = (2 * it) % C::kSlots, sd = (2 * it + 1) % C::kSlots;
+        int g = 0;
+        for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+         const BwdItem t = bwd_item<CAUSAL>(p, item);
+         for (int it = 0; ok && it < t.n_it; ++it, ++g) {
+          const int sq = (2 * g) % C::kSlots, sd = (2 * g + 1) % C::kSlots;
           // dV += P^T dO_i as soon as the elementwise warps have written P^T
           // (P^T of query group kk sits at S^T column 16 kk) and dP^T, which
           // also reads dO_i, is complete (so dO_i has landed, and its slot can
           // be released after dV); this frees the S^T columns for the next
           // block's scores
-          if (!wait_bounded_inl(&bar->dp_full, it & 1, ctx, kSiteBwdEw)) break;
-          if (!wait_bounded_inl(&bar->p_done, it & 1, ctx, kSiteBwdEw)) break;
+          ok = wait_bounded_inl(&bar->dp_full, g & 1, ctx, kSiteBwdEw) &&
+               wait_bounded_inl(&bar->p_done, g & 1, ctx, kSiteBwdEw);
+          if (!ok) break;
           tc_fence_after();
           const uint64_t dodesc_mn = sdesc_sw128(ring + sd * C::kTileBytes, 16384, 1024);
 #pragma unroll
@@ -428,7 +491,7 @@ __global__ void __launch_bounds__(512, 1)
           // reducers to take dQ out of these columns.  With a three-slot ring
           // dK goes first, because the next dO tile can only be loaded once
           // dK has released Q_i's slot.
-          if (!wait_bounded_inl(&bar->ew_done, it & 1, ctx, kSiteBwdEw)) break;
+          if (!(ok = wait_bounded_inl(&bar->ew_done, g & 1, ctx, kSiteBwdEw))) break;
           tc_fence_after();
           const uint64_t qdesc_mn = sdesc_sw128(ring + sq * C::kTileBytes, 16384, 1024);
           constexpr bool kDqFirst = C::kSlots > 3;
@@ -456,8 +519,10 @@ __global__ void __launch_bounds__(512, 1)
               mma_commit(&bar->dk_done);
             }
           }
+         }
+         // the item's dK and dV are complete, and its K and V read for the last time
+         if (ok) mma_commit(&bar->acc_done);
         }
-        mma_commit(&bar->acc_done);
         mma_commit(&bar->drain[1]);
         wait_drain_inl(&bar->drain[1], 0, kDrainLimitNs);
       }
@@ -468,14 +533,21 @@ __global__ void __launch_bounds__(512, 1)
     // ------------------------------------------------------------------ reducers
     // (no role without the atomic dQ: the warpgroup keeps its launch budget)
     if (kAtomicDq) {
-    setmaxnreg_inc<kBwdWorkRegs>();
+    setmaxnreg_inc<kBwdRedRegs>();
     const int q = warp & 3;
     const uint32_t tDQ = tmem + C::kDpCol + ((uint32_t)(q * 32) << 16);
     uint8_t* stage = sStage + q * 4096;
     const int chunk = lane & 7;
     constexpr int kChunks = D / 32;  // 32-column chunks of a dQ row
-    for (int it = 0; it < n_it; ++it) {
-      if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->dq_full, it & 1, ctx, kSiteBwdDq))) break;
+    bool alive = true;
+    int g = 0;
+    for (int item = blockIdx.x; alive && item < p.num_items; item += gridDim.x) {
+     const BwdItem t = bwd_item<CAUSAL>(p, item);
+     for (int it = 0; it < t.n_it; ++it, ++g) {
+      if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->dq_full, g & 1, ctx, kSiteBwdDq))) {
+        alive = false;
+        break;
+      }
       tc_fence_after();
       uint32_t dqv[kChunks][32];
 #pragma unroll
@@ -489,8 +561,8 @@ __global__ void __launch_bounds__(512, 1)
       // thread = query row 32 q + lane; each 32 x 32 block goes through the
       // stage (row-major, 16-byte chunks swizzled by row) and comes back with
       // 8 lanes per row, so that each reduction covers four whole 128-byte lines
-      const int qrow0 = (i_start + it) * 128 + 32 * q;
-      float* acc_rows = p.dq_acc + ((size_t)bh * N + qrow0) * D;
+      const int qrow0 = (t.i_start + it) * 128 + 32 * q;
+      float* acc_rows = p.dq_acc + ((size_t)t.bh * N + qrow0) * D;
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
@@ -506,36 +578,39 @@ __global__ void __launch_bounds__(512, 1)
         }
         __syncwarp();
       }
+     }
     }
     }
   } else {
     // ------------------------------------------------------------------ elementwise
     setmaxnreg_inc<kBwdWorkRegs>();
-    const int g = warp >> 2;
+    const int grp = warp >> 2;  // warpgroup: query columns [64 grp, 64 grp + 64)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + C::kSCol + lane_off;
     const uint32_t tDP = tmem + C::kDpCol + lane_off;
     const float sl2 = p.scale_log2;
-    uint8_t* ds_row = sDS + g * 16384 + r * 128;
+    uint8_t* ds_row = sDS + grp * 16384 + r * 128;
     bool alive = true;
-    for (int it = 0; alive && it < n_it; ++it) {
-      const int i = i_start + it;
-      const float* stat = reinterpret_cast<const float*>(sStat + (it % C::kStatEntries) * C::kStatBytes);
+    int g = 0, w = 0;
+    for (int item = blockIdx.x; alive && item < p.num_items; item += gridDim.x, ++w) {
+     const BwdItem t = bwd_item<CAUSAL>(p, item);
+     for (int it = 0; alive && it < t.n_it; ++it, ++g) {
+      const float* stat = reinterpret_cast<const float*>(sStat + (g % C::kStatEntries) * C::kStatBytes);
       // ---- phase 1: P^T = 2^(S^T c - L log2e) into TMEM, the fp32 values kept
       // in registers; issuer B starts dV as soon as all of P^T is written
-      if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->s_full, it & 1, ctx, kSiteBwdS))) {
+      if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->s_full, g & 1, ctx, kSiteBwdS))) {
         alive = false;
         break;
       }
       tc_fence_after();
-      const bool diag = CAUSAL && (i == jb);
+      const bool diag = CAUSAL && it == 0;  // with the mask the first query block is i = j
       const float2 c2 = make_float2(sl2, sl2);
       float2 pf[2][16];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
-        const int qc = 64 * g + 32 * ch;  // first query column of this chunk
+        const int qc = 64 * grp + 32 * ch;  // first query column of this chunk
         uint32_t sv[32];
         tmem_ld32(tS + qc, sv);
         tmem_wait_ld();
@@ -571,8 +646,8 @@ __global__ void __launch_bounds__(512, 1)
       // once the previous block's dK and dQ have read it (dP^T of this block
       // was issued after the reducers took the previous dQ out of TMEM; dK,
       // which runs after dQ, reports on its own)
-      bool ok2 = wait_bounded_inl(&bar->dp_full, it & 1, ctx, kSiteBwdDp);
-      if (it > 0) ok2 = ok2 && wait_bounded_inl(&bar->dk_done, (it - 1) & 1, ctx, kSiteBwdDp);
+      bool ok2 = wait_bounded_inl(&bar->dp_full, g & 1, ctx, kSiteBwdDp);
+      if (g > 0) ok2 = ok2 && wait_bounded_inl(&bar->dk_done, (g - 1) & 1, ctx, kSiteBwdDp);
       if (!__all_sync(0xffffffffu, ok2)) {
         alive = false;
         break;
@@ -580,7 +655,7 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_after();
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
-        const int qc = 64 * g + 32 * ch;
+        const int qc = 64 * grp + 32 * ch;
         uint32_t dp[32];
         tmem_ld32(tDP + qc, dp);
         tmem_wait_ld();
@@ -598,7 +673,7 @@ __global__ void __launch_bounds__(512, 1)
             dk[2 * e4 + h] = pack_bf16x2(dse.x, dse.y);
           }
         }
-        // dS^T row r, queries [qc, qc+32): 4 chunks of 16 B in the swizzled atom g
+        // dS^T row r, queries [qc, qc+32): 4 chunks of 16 B in the swizzled atom grp
 #pragma unroll
         for (int c16 = 0; c16 < 4; ++c16) {
           const int chunk = ((qc & 63) >> 3) + c16;
@@ -609,14 +684,21 @@ __global__ void __launch_bounds__(512, 1)
       fence_async_shared();
       tc_fence_before();
       mbar_arrive(&bar->ew_done);
-    }
-    // ---- epilogue: warpgroup 0 writes dK = scale dK_acc, warpgroup 1 writes dV
-    if (alive && __all_sync(0xffffffffu, wait_bounded_inl(&bar->acc_done, 0, ctx, kSiteBwdAcc))) {
+     }
+     // ---- epilogue: warpgroup 0 writes dK = scale dK_acc, warpgroup 1 writes
+     // dV.  The next item's first dV and dK overwrite these columns only
+     // after this warpgroup's next p_done arrival, which follows these reads.
+     if (!alive || !__all_sync(0xffffffffu, wait_bounded_inl(&bar->acc_done, w & 1, ctx, kSiteBwdAcc))) {
+      alive = false;
+      break;
+     }
+     {
       tc_fence_after();
-      const uint32_t tAcc = tmem + (g ? C::kDvCol : C::kDkCol) + lane_off;
-      const float mul = g ? 1.f : p.scale;
-      const int kg = k0 + r;
-      __nv_bfloat16* out = (g ? p.dv_out : p.dk_out) + ((size_t)bh * N + kg) * D;
+      const uint32_t tAcc = tmem + (grp ? C::kDvCol : C::kDkCol) + lane_off;
+      const float mul = grp ? 1.f : p.scale;
+      const BwdItem e = bwd_item<CAUSAL>(p, item);
+      const int kg = e.jb * 128 + r;
+      __nv_bfloat16* out = (grp ? p.dv_out : p.dk_out) + ((size_t)e.bh * N + kg) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
@@ -627,15 +709,16 @@ __global__ void __launch_bounds__(512, 1)
           uint4* o4 = reinterpret_cast<uint4*>(out + 32 * c);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
-            w.y = pack_bf16x2(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
-            w.z = pack_bf16x2(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
-            w.w = pack_bf16x2(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
-            o4[v4] = w;
+            uint4 w4;
+            w4.x = pack_bf16x2(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
+            w4.y = pack_bf16x2(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
+            w4.z = pack_bf16x2(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
+            w4.w = pack_bf16x2(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
+            o4[v4] = w4;
           }
         }
       }
+     }
     }
   }
 

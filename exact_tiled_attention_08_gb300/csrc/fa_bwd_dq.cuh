@@ -69,6 +69,8 @@ struct BwdDqParams {
   __nv_bfloat16* dq;
   int N;
   int nqb;           // query (and key) blocks per head
+  int num_bh;        // batch * heads
+  int group_heads;   // with the mask: heads per group of the item order
   float scale_log2;  // scale * log2(e)
   float scale;
   uint64_t wait_limit_ns;
@@ -98,9 +100,23 @@ __global__ void __launch_bounds__(384, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N;
-  // query blocks of a head from the last (the most key blocks when causal) to the first
-  const int ib = p.nqb - 1 - (int)(blockIdx.x % p.nqb);
-  const int bh = (int)(blockIdx.x / p.nqb);
+  // query blocks from the last (the most key blocks when causal) to the
+  // first: without the mask head by head; with it in groups of group_heads
+  // heads, by query block first inside a group (the costliest block of every
+  // head of the group, then the next), so that the hardware hands the
+  // costliest CTAs out first while a group's K and V still fit in L2
+  int ib, bh;
+  if (CAUSAL) {
+    const int per_group = p.group_heads * p.nqb;
+    const int grp = (int)blockIdx.x / per_group;
+    const int r = (int)blockIdx.x - grp * per_group;
+    const int gh = min(p.group_heads, p.num_bh - grp * p.group_heads);
+    ib = p.nqb - 1 - r / gh;
+    bh = grp * p.group_heads + r % gh;
+  } else {
+    ib = p.nqb - 1 - (int)(blockIdx.x % p.nqb);
+    bh = (int)(blockIdx.x / p.nqb);
+  }
   const int q0 = ib * 128;
   const int nb = CAUSAL ? ib + 1 : p.nqb;  // key blocks visited
 

@@ -136,6 +136,19 @@ fa_status launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   return FA_OK;
 }
 
+// Heads per group of the causal item order of the backward kernels: the
+// smallest divisor of the head count whose group holds at least four times
+// the SMs' worth of the costliest item (so that a group's costliest items,
+// handed out first, finish well before the group's one-block items run out),
+// or all heads.  Groups of G heads keep the working set (G heads' Q and dO,
+// or K and V) small enough for L2.
+int causal_group_heads(int BH, int nblk, int sms) {
+  const long long need = (4LL * sms + nblk) / (nblk + 1);  // ceil(4 sms / (nblk + 1))
+  for (int g = 1; g < BH; ++g)
+    if (BH % g == 0 && g >= need) return g;
+  return BH;
+}
+
 template <int D, bool CAUSAL, bool ATOMIC_DQ>
 fa_status launch_bwd(const CUtensorMap* maps, const fa::BwdParams& p, int BH, cudaStream_t stream) {
   using C = fa::BwdCfg<D, ATOMIC_DQ>;
@@ -145,11 +158,24 @@ fa_status launch_bwd(const CUtensorMap* maps, const fa::BwdParams& p, int BH, cu
   // (setmaxnreg); that only works if the block really gets 128 per thread
   cudaFuncAttributes attr;
   if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess || attr.numRegs != C::kLaunchRegs) return FA_ERR_CUDA;
-  const long long grid = (long long)p.nkb * BH;
+  // Without the mask every (key block, head) item costs the same: persistent
+  // CTAs, one per SM, walk the items, and each overlaps one item's last dQ
+  // reduction and dK/dV write with the next item's K/V load and first
+  // products.  With the mask the items' costs range from 1 to nkb query
+  // blocks, and one CTA per item lets the hardware balance them.
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return FA_ERR_CUDA;
+  fa::BwdParams q = p;
+  q.num_items = p.nkb * BH;
+  q.num_bh = BH;
+  q.group_heads = causal_group_heads(BH, p.nkb, sms);
+  const long long grid = (!CAUSAL && q.num_items > sms) ? sms : q.num_items;
   const TimingEvents ev = timing_events();
   if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_start, stream) != cudaSuccess) return FA_ERR_CUDA;
   kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                                                                  p);
+                                                                  q);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_stop, stream) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
@@ -160,8 +186,15 @@ fa_status launch_bwd_dq(const CUtensorMap* maps, const fa::BwdDqParams& p, int B
   using C = fa::BwdDqCfg<D>;
   auto kernel = fa::fa_bwd_dq_kernel<D, CAUSAL>;
   if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return FA_ERR_CUDA;
+  fa::BwdDqParams q = p;
+  q.num_bh = BH;
+  q.group_heads = causal_group_heads(BH, p.nqb, sms);
   const long long grid = (long long)p.nqb * BH;
-  kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+  kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], q);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -75,6 +75,48 @@ def test_backward_several_heads_and_batches(causal):
 
 
 @pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [128, 300])
+def test_backward_ctas_over_several_items(N, d):
+    """Without the mask the backward's CTAs stay resident, one per SM, and walk
+    the (key block, batch, head) items; with about 2.5 items per SM most CTAs
+    take two or three, carrying barrier phases, ring positions and statistics
+    entries from one item to the next.  Every head is checked, for fa_bwd and
+    for fa_bwd_deterministic (whose dK and dV come from the same kernel)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nkb = (N + 127) // 128
+    H = -(-5 * sms // (2 * nkb))
+    inp = make_inputs(1, H, N, d, seed=25 + N + d)
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = (inp[x].cuda() for x in ("q", "k", "v", "do"))
+    o, lse = fa.attention_forward(q, k, v, scale, False)
+    runs = [fa.attention_backward(q, k, v, o, do, lse, scale, False, deterministic=det) for det in (False, True)]
+    st = fa.fa_check_device_status()
+    assert st == fa.FA_OK, fa.fa_status_string(st)
+    check_grads(inp, runs[0], scale, False)
+    # the deterministic dQ against the oracle; dK, dV bit for bit as fa_bwd's
+    check_grads(inp, (runs[1][0], runs[0][1], runs[0][2]), scale, False)
+    assert torch.equal(runs[0][1], runs[1][1]) and torch.equal(runs[0][2], runs[1][2])
+
+
+def test_backward_causal_item_groups():
+    """With the mask the key-block items run in groups of heads, costliest key
+    block first inside a group.  B = 2, H = 72, N = 1024 (8 key blocks) gives
+    two groups of 72 heads on a 152-SM part (the smallest divisor of 144 that
+    is at least 4 x 152 / 9); every head is checked, for fa_bwd and for
+    fa_bwd_deterministic (whose dQ pass orders its query blocks the same way)."""
+    inp = make_inputs(2, 72, 1024, 64, seed=26)
+    scale = 1.0 / math.sqrt(64)
+    q, k, v, do = (inp[x].cuda() for x in ("q", "k", "v", "do"))
+    o, lse = fa.attention_forward(q, k, v, scale, True)
+    runs = [fa.attention_backward(q, k, v, o, do, lse, scale, True, deterministic=det) for det in (False, True)]
+    st = fa.fa_check_device_status()
+    assert st == fa.FA_OK, fa.fa_status_string(st)
+    check_grads(inp, runs[0], scale, True)
+    check_grads(inp, (runs[1][0], runs[0][1], runs[0][2]), scale, True)
+    assert torch.equal(runs[0][1], runs[1][1]) and torch.equal(runs[0][2], runs[1][2])
+
+
+@pytest.mark.parametrize("d", [64, 128])
 def test_backward_rescale_stress(d):
     inp = make_inputs(2, 2, 1024, d, seed=22, key_outliers=True)
     scale = 1.0 / math.sqrt(d)
