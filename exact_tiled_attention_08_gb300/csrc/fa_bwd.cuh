@@ -114,14 +114,14 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------------------
 // main backward kernel: the work is one item per (key block j, batch, head).
 // With the causal mask one CTA runs per item (the items' costs range from 1
-// to nkb query blocks, and the hardware's CTA scheduler balances them);
-// without it the CTAs are persistent, one per SM, and walk the items
-// blockIdx.x, blockIdx.x + gridDim.x, ...  All pipeline counters (ring
-// fills, per-block barrier phases, statistics entries) run on across the
-// items, so a CTA loads the next item's first Q tile while the current item
-// finishes, its K and V as soon as the last dK and dQ products have read the
-// old ones, and the reducers' last dQ_i and the dK, dV write-out overlap with
-// the next item's first products.
+// to nkb query blocks; bwd_item hands the costliest out first and the
+// hardware's CTA scheduler balances them); without it the CTAs are
+// persistent, one per SM, and walk the items blockIdx.x, blockIdx.x +
+// gridDim.x, ...  All pipeline counters (ring fills, per-block barrier
+// phases, statistics entries) run on across the items: a CTA loads the next
+// item's K and V, then its first Q tile, as soon as the current item's last
+// dK and dQ products have read the old K and V, and the reducers' last dQ_i
+// and the dK, dV write-out overlap with the next item's first products.
 //
 // K_j and V_j (128 keys) stay in shared memory; the query blocks i (all of
 // them, or i >= j when causal) stream Q_i (with its rows' LSE log2(e) and
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(256)
 // while the next query block is processed.  The elementwise step is split in
 // two so that dV runs while dS^T is computed, and the next block's S^T (whose
 // columns dV frees) while dK and dQ run.  dK, dV accumulate in TMEM across
-// all query blocks and are written once at the end.
+// the item's query blocks and are written once at the end of the item.
 //
 // The global fp32 reduction of dQ_i (64 KB per query block at d = 128) is
 // bound by the L2's atomic throughput, which is close to the time the rest of
