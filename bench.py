@@ -390,7 +390,8 @@ def run_ours(args, rank, world, local):
                "note": "fa_fwd_fp8: Q, K rotated and quantised per 128-row block, V per channel, E4M3 products; "
                        "the call includes the operand preparation"}
 
-    step_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    step_times = [e[0].elapsed_time(e[1]) for e in ev]
+    step_ms = statistics.mean(step_times)
     fwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
     bwd_ms = statistics.mean(e[4].elapsed_time(e[5]) for e in ev)
     step_ms_max = max_over_ranks(step_ms, world)
@@ -483,6 +484,16 @@ def run_ours(args, rank, world, local):
         return
     peaks, peak_source = load_peaks()
     fwd_tf = fwd_flops / (fwd_ms / 1e3) / 1e12
+    # exponentials: one per score in the forward (N^2 per head, half with the
+    # mask), against the MUFU's 32 ex2 per clock per SM (probe) x SMs x the
+    # median SM clock sampled under load
+    fwd_exps = w.fwd_flops() / (4.0 * w.d)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ex2_peak = 32.0 * sms * clock_info["sm_mhz"] * 1e6 if clock_info.get("sm_mhz") else None
+    exp_rate = {"fwd_exps_per_s": fwd_exps / (fwd_ms / 1e3), "ex2_peak_per_s": ex2_peak,
+                "frac": (fwd_exps / (fwd_ms / 1e3) / ex2_peak) if ex2_peak else None,
+                "note": "N^2 exponentials per head (half with the mask) over the forward kernel's time; "
+                        "peak = 32 ex2 per clock per SM x SMs x median SM clock"}
     bwd_tf = bwd_main_flops / (bwd_ms / 1e3) / 1e12
     # dominant kernel: the one with the larger share of the step
     if bwd_ms >= fwd_ms:
@@ -507,6 +518,8 @@ def run_ours(args, rank, world, local):
         "roofline": roofline,
         "breakdown": {"fwd_kernel_ms": fwd_ms, "fwd_tflops": fwd_tf, "bwd_kernel_ms": bwd_ms, "bwd_tflops": bwd_tf,
                       "other_ms": step_ms - fwd_ms - bwd_ms,
+                      "step_ms_median": statistics.median(step_times), "step_ms_best": min(step_times),
+                      "fwd_exp_rate": exp_rate,
                       "fwd_frac_of_sustained_peak": fwd_tf / peak, "bwd_frac_of_sustained_peak": bwd_tf / peak,
                       "fp8_forward": fp8},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
