@@ -338,49 +338,49 @@ __global__ void __launch_bounds__(512, 1)
         int fill = 0, g = 0, w = 0, kv_loads = 0;
         bool ok = true;
         for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x, ++w) {
-         const BwdItem t = bwd_item<CAUSAL>(p, item);
-         for (int it = 0; ok && it < t.n_it; ++it, ++g) {
-          const int i = t.i_start + it;
-          for (int which = 0; which < 2; ++which) {
-            // K and V of the item go first, once the previous item's last
-            // products (acc_done) have read the old ones
-            if (!which && it == 0) {
-              if (w > 0 && !wait_bounded_inl(&bar->acc_done, (w - 1) & 1, ctx, kSiteBwdProducer)) {
+          const BwdItem t = bwd_item<CAUSAL>(p, item);
+          for (int it = 0; ok && it < t.n_it; ++it, ++g) {
+            const int i = t.i_start + it;
+            for (int which = 0; which < 2; ++which) {
+              // K and V of the item go first, once the previous item's last
+              // products (acc_done) have read the old ones
+              if (!which && it == 0) {
+                if (w > 0 && !wait_bounded_inl(&bar->acc_done, (w - 1) & 1, ctx, kSiteBwdProducer)) {
+                  ok = false;
+                  break;
+                }
+                mbar_arrive_expect_tx(&bar->kv_full, 2 * C::kTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a) {
+                  tma_load_3d(sK + a * 16384, &map_k, &bar->kv_full, a * 64, t.jb * 128, t.bh);
+                  tma_load_3d(sV + a * 16384, &map_v, &bar->kv_full, a * 64, t.jb * 128, t.bh);
+                }
+                ++kv_loads;
+              }
+              const int s = fill % C::kSlots;
+              const uint32_t u = fill / C::kSlots;
+              if (!wait_bounded_inl(&bar->ring_empty[s], (u & 1) ^ 1, ctx, kSiteBwdProducer)) {
                 ok = false;
                 break;
               }
-              mbar_arrive_expect_tx(&bar->kv_full, 2 * C::kTileBytes);
-              for (int a = 0; a < C::kAtoms; ++a) {
-                tma_load_3d(sK + a * 16384, &map_k, &bar->kv_full, a * 64, t.jb * 128, t.bh);
-                tma_load_3d(sV + a * 16384, &map_v, &bar->kv_full, a * 64, t.jb * 128, t.bh);
+              mbar_arrive_expect_tx(&bar->ring_full[s], C::kTileBytes + (which ? 0 : C::kStatBytes));
+              const CUtensorMap* map = which ? &map_do : &map_q;
+              for (int a = 0; a < C::kAtoms; ++a)
+                tma_load_3d(sRing + s * C::kTileBytes + a * 16384, map, &bar->ring_full[s], a * 64, i * 128, t.bh);
+              // with a three-slot ring the same tile of the next query block goes
+              // to L2 now, so that its load (which waits for a free slot) is
+              // served from L2
+              if (C::kSlots < 4 && it + 1 < t.n_it)
+                for (int a = 0; a < C::kAtoms; ++a) tma_prefetch_l2_3d(map, a * 64, (i + 1) * 128, t.bh);
+              if (!which) {
+                // the entry was last read by the elementwise step of block
+                // g - kStatEntries, which has finished once this slot is free
+                uint8_t* st = sStat + (g % C::kStatEntries) * C::kStatBytes;
+                tma_load_2d(st, &map_lse2, &bar->ring_full[s], i * 128, t.bh);
+                tma_load_2d(st + 512, &map_delta, &bar->ring_full[s], i * 128, t.bh);
               }
-              ++kv_loads;
+              ++fill;
             }
-            const int s = fill % C::kSlots;
-            const uint32_t u = fill / C::kSlots;
-            if (!wait_bounded_inl(&bar->ring_empty[s], (u & 1) ^ 1, ctx, kSiteBwdProducer)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&bar->ring_full[s], C::kTileBytes + (which ? 0 : C::kStatBytes));
-            const CUtensorMap* map = which ? &map_do : &map_q;
-            for (int a = 0; a < C::kAtoms; ++a)
-              tma_load_3d(sRing + s * C::kTileBytes + a * 16384, map, &bar->ring_full[s], a * 64, i * 128, t.bh);
-            // with a three-slot ring the same tile of the next query block goes
-            // to L2 now, so that its load (which waits for a free slot) is
-            // served from L2
-            if (C::kSlots < 4 && it + 1 < t.n_it)
-              for (int a = 0; a < C::kAtoms; ++a) tma_prefetch_l2_3d(map, a * 64, (i + 1) * 128, t.bh);
-            if (!which) {
-              // the entry was last read by the elementwise step of block
-              // g - kStatEntries, which has finished once this slot is free
-              uint8_t* st = sStat + (g % C::kStatEntries) * C::kStatBytes;
-              tma_load_2d(st, &map_lse2, &bar->ring_full[s], i * 128, t.bh);
-              tma_load_2d(st + 512, &map_delta, &bar->ring_full[s], i * 128, t.bh);
-            }
-            ++fill;
           }
-         }
         }
         if (kv_loads > 0) wait_drain_inl(&bar->kv_full, (kv_loads - 1) & 1, kDrainLimitNs);
         for (int s = 0; s < C::kSlots; ++s) {
@@ -406,47 +406,56 @@ __global__ void __launch_bounds__(512, 1)
         // g counts query blocks over all of the CTA's items, w the items.
         int g = 0, w = 0;
         for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x, ++w) {
-         const BwdItem t = bwd_item<CAUSAL>(p, item);
-         ok = wait_bounded_inl(&bar->kv_full, w & 1, ctx, kSiteBwdKV);
-         for (int it = 0; ok && it < t.n_it; ++it, ++g) {
+          const BwdItem t = bwd_item<CAUSAL>(p, item);
+          ok = wait_bounded_inl(&bar->kv_full, w & 1, ctx, kSiteBwdKV);
+          for (int it = 0; ok && it < t.n_it; ++it, ++g) {
 #pragma unroll
-          for (int step = 0; step < 2; ++step) {
-            if (step == 0) {
-              // S^T = K Q_i^T, once dV has consumed the previous P^T held in
-              // these columns
-              const int fq = 2 * g, sq = fq % C::kSlots;
-              if (!wait_bounded_inl(&bar->ring_full[sq], (fq / C::kSlots) & 1, ctx, kSiteBwdQ)) { ok = false; break; }
-              if (g > 0 && !wait_bounded_inl(&bar->dv_done, (g - 1) & 1, ctx, kSiteBwdDvDone)) { ok = false; break; }
-              tc_fence_after();
-              const uint64_t qdesc = sdesc_sw128(ring + sq * C::kTileBytes, 16, 1024);
+            for (int step = 0; step < 2; ++step) {
+              if (step == 0) {
+                // S^T = K Q_i^T, once dV has consumed the previous P^T held in
+                // these columns
+                const int fq = 2 * g, sq = fq % C::kSlots;
+                if (!wait_bounded_inl(&bar->ring_full[sq], (fq / C::kSlots) & 1, ctx, kSiteBwdQ)) {
+                  ok = false;
+                  break;
+                }
+                if (g > 0 && !wait_bounded_inl(&bar->dv_done, (g - 1) & 1, ctx, kSiteBwdDvDone)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint64_t qdesc = sdesc_sw128(ring + sq * C::kTileBytes, 16, 1024);
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                mma_bf16_ss(tS, kdesc + off, qdesc + off, id_s, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(&bar->s_full);
-            } else {
-              // dP^T = V dO_i^T, once the reducers have taken the previous dQ
-              // out of these columns (without dQ: once the elementwise step
-              // has read the previous dP^T)
-              const int fd = 2 * g + 1, sd = fd % C::kSlots;
-              if (!wait_bounded_inl(&bar->ring_full[sd], (fd / C::kSlots) & 1, ctx, kSiteBwdDo)) { ok = false; break; }
-              if (g > 0 && !wait_bounded_inl(kAtomicDq ? &bar->dq_free : &bar->ew_done, (g - 1) & 1, ctx,
-                                             kSiteBwdDqFree)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint64_t dodesc = sdesc_sw128(ring + sd * C::kTileBytes, 16, 1024);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                  const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                  mma_bf16_ss(tS, kdesc + off, qdesc + off, id_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar->s_full);
+              } else {
+                // dP^T = V dO_i^T, once the reducers have taken the previous dQ
+                // out of these columns (without dQ: once the elementwise step
+                // has read the previous dP^T)
+                const int fd = 2 * g + 1, sd = fd % C::kSlots;
+                if (!wait_bounded_inl(&bar->ring_full[sd], (fd / C::kSlots) & 1, ctx, kSiteBwdDo)) {
+                  ok = false;
+                  break;
+                }
+                if (g > 0 && !wait_bounded_inl(kAtomicDq ? &bar->dq_free : &bar->ew_done, (g - 1) & 1, ctx,
+                                               kSiteBwdDqFree)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint64_t dodesc = sdesc_sw128(ring + sd * C::kTileBytes, 16, 1024);
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                mma_bf16_ss(tDP, vdesc + off, dodesc + off, id_s, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                  const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                  mma_bf16_ss(tDP, vdesc + off, dodesc + off, id_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar->dp_full);
               }
-              mma_commit(&bar->dp_full);
             }
           }
-         }
         }
         mma_commit(&bar->drain[0]);
         wait_drain_inl(&bar->drain[0], 0, kDrainLimitNs);
@@ -466,62 +475,62 @@ __global__ void __launch_bounds__(512, 1)
         bool ok = true;
         int g = 0;
         for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
-         const BwdItem t = bwd_item<CAUSAL>(p, item);
-         for (int it = 0; ok && it < t.n_it; ++it, ++g) {
-          const int sq = (2 * g) % C::kSlots, sd = (2 * g + 1) % C::kSlots;
-          // dV += P^T dO_i as soon as the elementwise warps have written P^T
-          // (P^T of query group kk sits at S^T column 16 kk) and dP^T, which
-          // also reads dO_i, is complete (so dO_i has landed, and its slot can
-          // be released after dV); this frees the S^T columns for the next
-          // block's scores
-          ok = wait_bounded_inl(&bar->dp_full, g & 1, ctx, kSiteBwdEw) &&
-               wait_bounded_inl(&bar->p_done, g & 1, ctx, kSiteBwdEw);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t dodesc_mn = sdesc_sw128(ring + sd * C::kTileBytes, 16384, 1024);
+          const BwdItem t = bwd_item<CAUSAL>(p, item);
+          for (int it = 0; ok && it < t.n_it; ++it, ++g) {
+            const int sq = (2 * g) % C::kSlots, sd = (2 * g + 1) % C::kSlots;
+            // dV += P^T dO_i as soon as the elementwise warps have written P^T
+            // (P^T of query group kk sits at S^T column 16 kk) and dP^T, which
+            // also reads dO_i, is complete (so dO_i has landed, and its slot can
+            // be released after dV); this frees the S^T columns for the next
+            // block's scores
+            ok = wait_bounded_inl(&bar->dp_full, g & 1, ctx, kSiteBwdEw) &&
+                 wait_bounded_inl(&bar->p_done, g & 1, ctx, kSiteBwdEw);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t dodesc_mn = sdesc_sw128(ring + sd * C::kTileBytes, 16384, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tDV, tS + kk * 16, dodesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
-                        (it > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bar->dv_done);
-          mma_commit(&bar->ring_empty[sd]);
-          // dQ_i = dS K (into the dP^T columns, read by now) and dK += dS^T Q_i,
-          // once dS^T is written.  dQ goes first when the ring is deep enough
-          // to have the next dO tile already: the next dP^T waits for the
-          // reducers to take dQ out of these columns.  With a three-slot ring
-          // dK goes first, because the next dO tile can only be loaded once
-          // dK has released Q_i's slot.
-          if (!(ok = wait_bounded_inl(&bar->ew_done, g & 1, ctx, kSiteBwdEw))) break;
-          tc_fence_after();
-          const uint64_t qdesc_mn = sdesc_sw128(ring + sq * C::kTileBytes, 16384, 1024);
-          constexpr bool kDqFirst = C::kSlots > 3;
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ts(tDV, tS + kk * 16, dodesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
+                          (it > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bar->dv_done);
+            mma_commit(&bar->ring_empty[sd]);
+            // dQ_i = dS K (into the dP^T columns, read by now) and dK += dS^T Q_i,
+            // once dS^T is written.  dQ goes first when the ring is deep enough
+            // to have the next dO tile already: the next dP^T waits for the
+            // reducers to take dQ out of these columns.  With a three-slot ring
+            // dK goes first, because the next dO tile can only be loaded once
+            // dK has released Q_i's slot.
+            if (!(ok = wait_bounded_inl(&bar->ew_done, g & 1, ctx, kSiteBwdEw))) break;
+            tc_fence_after();
+            const uint64_t qdesc_mn = sdesc_sw128(ring + sq * C::kTileBytes, 16384, 1024);
+            constexpr bool kDqFirst = C::kSlots > 3;
 #pragma unroll
-          for (int step = 0; step < 2; ++step) {
-            if ((step == 0) == kDqFirst) {
-              if (kAtomicDq) {
+            for (int step = 0; step < 2; ++step) {
+              if ((step == 0) == kDqFirst) {
+                if (kAtomicDq) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                  mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4),
-                              id_q, kk > 0 ? 1u : 0u);
-                mma_commit(&bar->dq_full);
+                  for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4),
+                                id_q, kk > 0 ? 1u : 0u);
+                  mma_commit(&bar->dq_full);
+                }
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                  const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                  mma_bf16_ss(tDK, dsdesc_k + off, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
+                              (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                // Q_i has been read by S^T (long complete) and dK: release its
+                // slot; the dS^T tile is free for the next elementwise step once
+                // dQ has read it as well (dq_free, which the next dP^T waits for)
+                mma_commit(&bar->ring_empty[sq]);
+                mma_commit(&bar->dk_done);
               }
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                mma_bf16_ss(tDK, dsdesc_k + off, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
-                            (it > 0 || kk > 0) ? 1u : 0u);
-              }
-              // Q_i has been read by S^T (long complete) and dK: release its
-              // slot; the dS^T tile is free for the next elementwise step once
-              // dQ has read it as well (dq_free, which the next dP^T waits for)
-              mma_commit(&bar->ring_empty[sq]);
-              mma_commit(&bar->dk_done);
             }
           }
-         }
-         // the item's dK and dV are complete, and its K and V read for the last time
-         if (ok) mma_commit(&bar->acc_done);
+          // the item's dK and dV are complete, and its K and V read for the last time
+          if (ok) mma_commit(&bar->acc_done);
         }
         mma_commit(&bar->drain[1]);
         wait_drain_inl(&bar->drain[1], 0, kDrainLimitNs);
@@ -542,43 +551,43 @@ __global__ void __launch_bounds__(512, 1)
     bool alive = true;
     int g = 0;
     for (int item = blockIdx.x; alive && item < p.num_items; item += gridDim.x) {
-     const BwdItem t = bwd_item<CAUSAL>(p, item);
-     for (int it = 0; it < t.n_it; ++it, ++g) {
-      if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->dq_full, g & 1, ctx, kSiteBwdDq))) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t dqv[kChunks][32];
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) tmem_ld32(tDQ + 32 * c, dqv[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) reg_fence32(dqv[c]);
-      // dQ_i is in registers: issuer A may overwrite these columns with dP^T
-      tc_fence_before();
-      mbar_arrive(&bar->dq_free);
-      // thread = query row 32 q + lane; each 32 x 32 block goes through the
-      // stage (row-major, 16-byte chunks swizzled by row) and comes back with
-      // 8 lanes per row, so that each reduction covers four whole 128-byte lines
-      const int qrow0 = (t.i_start + it) * 128 + 32 * q;
-      float* acc_rows = p.dq_acc + ((size_t)t.bh * N + qrow0) * D;
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-#pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16)
-          *reinterpret_cast<uint4*>(stage + lane * 128 + ((c16 ^ (lane & 7)) << 4)) =
-              make_uint4(dqv[c][4 * c16], dqv[c][4 * c16 + 1], dqv[c][4 * c16 + 2], dqv[c][4 * c16 + 3]);
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int row = 4 * k + (lane >> 3);
-          const float4 x = *reinterpret_cast<const float4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4));
-          if (qrow0 + row < N) red_add_v4(acc_rows + (size_t)row * D + 32 * c + 4 * chunk, x.x, x.y, x.z, x.w);
+      const BwdItem t = bwd_item<CAUSAL>(p, item);
+      for (int it = 0; it < t.n_it; ++it, ++g) {
+        if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->dq_full, g & 1, ctx, kSiteBwdDq))) {
+          alive = false;
+          break;
         }
-        __syncwarp();
+        tc_fence_after();
+        uint32_t dqv[kChunks][32];
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) tmem_ld32(tDQ + 32 * c, dqv[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) reg_fence32(dqv[c]);
+        // dQ_i is in registers: issuer A may overwrite these columns with dP^T
+        tc_fence_before();
+        mbar_arrive(&bar->dq_free);
+        // thread = query row 32 q + lane; each 32 x 32 block goes through the
+        // stage (row-major, 16-byte chunks swizzled by row) and comes back with
+        // 8 lanes per row, so that each reduction covers four whole 128-byte lines
+        const int qrow0 = (t.i_start + it) * 128 + 32 * q;
+        float* acc_rows = p.dq_acc + ((size_t)t.bh * N + qrow0) * D;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+          for (int c16 = 0; c16 < 8; ++c16)
+            *reinterpret_cast<uint4*>(stage + lane * 128 + ((c16 ^ (lane & 7)) << 4)) =
+                make_uint4(dqv[c][4 * c16], dqv[c][4 * c16 + 1], dqv[c][4 * c16 + 2], dqv[c][4 * c16 + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int row = 4 * k + (lane >> 3);
+            const float4 x = *reinterpret_cast<const float4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4));
+            if (qrow0 + row < N) red_add_v4(acc_rows + (size_t)row * D + 32 * c + 4 * chunk, x.x, x.y, x.z, x.w);
+          }
+          __syncwarp();
+        }
       }
-     }
     }
     }
   } else {
@@ -595,130 +604,130 @@ __global__ void __launch_bounds__(512, 1)
     bool alive = true;
     int g = 0, w = 0;
     for (int item = blockIdx.x; alive && item < p.num_items; item += gridDim.x, ++w) {
-     const BwdItem t = bwd_item<CAUSAL>(p, item);
-     for (int it = 0; alive && it < t.n_it; ++it, ++g) {
-      const float* stat = reinterpret_cast<const float*>(sStat + (g % C::kStatEntries) * C::kStatBytes);
-      // ---- phase 1: P^T = 2^(S^T c - L log2e) into TMEM, the fp32 values kept
-      // in registers; issuer B starts dV as soon as all of P^T is written
-      if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->s_full, g & 1, ctx, kSiteBwdS))) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
-      const bool diag = CAUSAL && it == 0;  // with the mask the first query block is i = j
-      const float2 c2 = make_float2(sl2, sl2);
-      float2 pf[2][16];
+      const BwdItem t = bwd_item<CAUSAL>(p, item);
+      for (int it = 0; alive && it < t.n_it; ++it, ++g) {
+        const float* stat = reinterpret_cast<const float*>(sStat + (g % C::kStatEntries) * C::kStatBytes);
+        // ---- phase 1: P^T = 2^(S^T c - L log2e) into TMEM, the fp32 values kept
+        // in registers; issuer B starts dV as soon as all of P^T is written
+        if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->s_full, g & 1, ctx, kSiteBwdS))) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        const bool diag = CAUSAL && it == 0;  // with the mask the first query block is i = j
+        const float2 c2 = make_float2(sl2, sl2);
+        float2 pf[2][16];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int qc = 64 * grp + 32 * ch;  // first query column of this chunk
-        uint32_t sv[32];
-        tmem_ld32(tS + qc, sv);
-        tmem_wait_ld();
-        reg_fence32(sv);
-        uint32_t pk[16];
+        for (int ch = 0; ch < 2; ++ch) {
+          const int qc = 64 * grp + 32 * ch;  // first query column of this chunk
+          uint32_t sv[32];
+          tmem_ld32(tS + qc, sv);
+          tmem_wait_ld();
+          reg_fence32(sv);
+          uint32_t pk[16];
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          // four queries' L*log2e (the same for every thread: a broadcast read)
-          const float4 l4 = *reinterpret_cast<const float4*>(stat + qc + 4 * e4);
+          for (int e4 = 0; e4 < 8; ++e4) {
+            // four queries' L*log2e (the same for every thread: a broadcast read)
+            const float4 l4 = *reinterpret_cast<const float4*>(stat + qc + 4 * e4);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = 4 * e4 + 2 * h;  // two queries at a time (packed fp32x2 arithmetic)
-            const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
-            const float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nl);
-            float2 pe = make_float2(ex2_approx(xs.x), ex2_approx(xs.y));
-            if (diag) {  // key k0 + r is in the future of query qbase + qc + e
-              if (qc + e < r) pe.x = 0.f;
-              if (qc + e + 1 < r) pe.y = 0.f;
+            for (int h = 0; h < 2; ++h) {
+              const int e = 4 * e4 + 2 * h;  // two queries at a time (packed fp32x2 arithmetic)
+              const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+              const float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nl);
+              float2 pe = make_float2(ex2_approx(xs.x), ex2_approx(xs.y));
+              if (diag) {  // key k0 + r is in the future of query qbase + qc + e
+                if (qc + e < r) pe.x = 0.f;
+                if (qc + e + 1 < r) pe.y = 0.f;
+              }
+              pf[ch][e / 2] = pe;
+              pk[2 * e4 + h] = pack_bf16x2(pe.x, pe.y);
             }
-            pf[ch][e / 2] = pe;
-            pk[2 * e4 + h] = pack_bf16x2(pe.x, pe.y);
+          }
+          // P^T of query groups qc/16 and qc/16 + 1 over the first 8 of their own columns
+          tmem_st8(tS + qc, pk);
+          tmem_st8(tS + qc + 16, pk + 8);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar->p_done);
+
+        // ---- phase 2: dS^T = P^T o (dP^T - delta) into the shared dS^T tile,
+        // once the previous block's dK and dQ have read it (dP^T of this block
+        // was issued after the reducers took the previous dQ out of TMEM; dK,
+        // which runs after dQ, reports on its own)
+        bool ok2 = wait_bounded_inl(&bar->dp_full, g & 1, ctx, kSiteBwdDp);
+        if (g > 0) ok2 = ok2 && wait_bounded_inl(&bar->dk_done, (g - 1) & 1, ctx, kSiteBwdDp);
+        if (!__all_sync(0xffffffffu, ok2)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const int qc = 64 * grp + 32 * ch;
+          uint32_t dp[32];
+          tmem_ld32(tDP + qc, dp);
+          tmem_wait_ld();
+          reg_fence32(dp);
+          uint32_t dk[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(stat + 128 + qc + 4 * e4);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = 4 * e4 + 2 * h;
+              const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+              const float2 dpd = __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd);
+              const float2 dse = __fmul2_rn(pf[ch][e / 2], dpd);
+              dk[2 * e4 + h] = pack_bf16x2(dse.x, dse.y);
+            }
+          }
+          // dS^T row r, queries [qc, qc+32): 4 chunks of 16 B in the swizzled atom grp
+#pragma unroll
+          for (int c16 = 0; c16 < 4; ++c16) {
+            const int chunk = ((qc & 63) >> 3) + c16;
+            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
+                make_uint4(dk[4 * c16], dk[4 * c16 + 1], dk[4 * c16 + 2], dk[4 * c16 + 3]);
           }
         }
-        // P^T of query groups qc/16 and qc/16 + 1 over the first 8 of their own columns
-        tmem_st8(tS + qc, pk);
-        tmem_st8(tS + qc + 16, pk + 8);
+        fence_async_shared();
+        tc_fence_before();
+        mbar_arrive(&bar->ew_done);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bar->p_done);
-
-      // ---- phase 2: dS^T = P^T o (dP^T - delta) into the shared dS^T tile,
-      // once the previous block's dK and dQ have read it (dP^T of this block
-      // was issued after the reducers took the previous dQ out of TMEM; dK,
-      // which runs after dQ, reports on its own)
-      bool ok2 = wait_bounded_inl(&bar->dp_full, g & 1, ctx, kSiteBwdDp);
-      if (g > 0) ok2 = ok2 && wait_bounded_inl(&bar->dk_done, (g - 1) & 1, ctx, kSiteBwdDp);
-      if (!__all_sync(0xffffffffu, ok2)) {
+      // ---- epilogue: warpgroup 0 writes dK = scale dK_acc, warpgroup 1 writes
+      // dV.  The next item's first dV and dK overwrite these columns only
+      // after this warpgroup's next p_done arrival, which follows these reads.
+      if (!alive || !__all_sync(0xffffffffu, wait_bounded_inl(&bar->acc_done, w & 1, ctx, kSiteBwdAcc))) {
         alive = false;
         break;
       }
-      tc_fence_after();
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int qc = 64 * grp + 32 * ch;
-        uint32_t dp[32];
-        tmem_ld32(tDP + qc, dp);
-        tmem_wait_ld();
-        reg_fence32(dp);
-        uint32_t dk[16];
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(stat + 128 + qc + 4 * e4);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = 4 * e4 + 2 * h;
-            const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
-            const float2 dpd = __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd);
-            const float2 dse = __fmul2_rn(pf[ch][e / 2], dpd);
-            dk[2 * e4 + h] = pack_bf16x2(dse.x, dse.y);
-          }
-        }
-        // dS^T row r, queries [qc, qc+32): 4 chunks of 16 B in the swizzled atom grp
-#pragma unroll
-        for (int c16 = 0; c16 < 4; ++c16) {
-          const int chunk = ((qc & 63) >> 3) + c16;
-          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
-              make_uint4(dk[4 * c16], dk[4 * c16 + 1], dk[4 * c16 + 2], dk[4 * c16 + 3]);
-        }
-      }
-      fence_async_shared();
-      tc_fence_before();
-      mbar_arrive(&bar->ew_done);
-     }
-     // ---- epilogue: warpgroup 0 writes dK = scale dK_acc, warpgroup 1 writes
-     // dV.  The next item's first dV and dK overwrite these columns only
-     // after this warpgroup's next p_done arrival, which follows these reads.
-     if (!alive || !__all_sync(0xffffffffu, wait_bounded_inl(&bar->acc_done, w & 1, ctx, kSiteBwdAcc))) {
-      alive = false;
-      break;
-     }
-     {
-      tc_fence_after();
-      const uint32_t tAcc = tmem + (grp ? C::kDvCol : C::kDkCol) + lane_off;
-      const float mul = grp ? 1.f : p.scale;
-      const BwdItem e = bwd_item<CAUSAL>(p, item);
-      const int kg = e.jb * 128 + r;
-      __nv_bfloat16* out = (grp ? p.dv_out : p.dk_out) + ((size_t)e.bh * N + kg) * D;
+      {
+        tc_fence_after();
+        const uint32_t tAcc = tmem + (grp ? C::kDvCol : C::kDkCol) + lane_off;
+        const float mul = grp ? 1.f : p.scale;
+        const BwdItem e = bwd_item<CAUSAL>(p, item);
+        const int kg = e.jb * 128 + r;
+        __nv_bfloat16* out = (grp ? p.dv_out : p.dk_out) + ((size_t)e.bh * N + kg) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tAcc + 32 * c, v);
-        tmem_wait_ld();
-        reg_fence32(v);
-        if (kg < N) {
-          uint4* o4 = reinterpret_cast<uint4*>(out + 32 * c);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tAcc + 32 * c, v);
+          tmem_wait_ld();
+          reg_fence32(v);
+          if (kg < N) {
+            uint4* o4 = reinterpret_cast<uint4*>(out + 32 * c);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 w4;
-            w4.x = pack_bf16x2(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
-            w4.y = pack_bf16x2(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
-            w4.z = pack_bf16x2(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
-            w4.w = pack_bf16x2(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
-            o4[v4] = w4;
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w4;
+              w4.x = pack_bf16x2(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
+              w4.y = pack_bf16x2(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
+              w4.z = pack_bf16x2(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
+              w4.w = pack_bf16x2(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
+              o4[v4] = w4;
+            }
           }
         }
       }
-     }
     }
   }
 
