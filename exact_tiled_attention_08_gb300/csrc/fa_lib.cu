@@ -138,15 +138,21 @@ fa_status launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
 
 // Heads per group of the causal item order of the backward kernels: the
 // smallest divisor of the head count whose group holds at least four times
-// the SMs' worth of the costliest item (so that a group's costliest items,
-// handed out first, finish well before the group's one-block items run out),
-// or all heads.  Groups of G heads keep the working set (G heads' Q and dO,
-// or K and V) small enough for L2.
+// the SMs' worth of the costliest item (need = ceil(4 sms / (nblk + 1))
+// heads, so that a group's costliest items, handed out first, finish well
+// before the group's one-block items run out), or all heads.  Groups of few
+// heads keep the working set (their Q and dO, or K and V) small enough for
+// L2.  Divisors come in pairs (i, BH / i), so i up to sqrt(BH) finds them all.
 int causal_group_heads(int BH, int nblk, int sms) {
-  const long long need = (4LL * sms + nblk) / (nblk + 1);  // ceil(4 sms / (nblk + 1))
-  for (int g = 1; g < BH; ++g)
-    if (BH % g == 0 && g >= need) return g;
-  return BH;
+  const long long need = (4LL * sms + nblk) / (nblk + 1);
+  long long best = BH;
+  for (long long i = 1; i * i <= BH; ++i) {
+    if (BH % i) continue;
+    const long long j = BH / i;
+    if (i >= need && i < best) best = i;
+    if (j >= need && j < best) best = j;
+  }
+  return (int)best;
 }
 
 template <int D, bool CAUSAL, bool ATOMIC_DQ>
