@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <initializer_list>
 #include <mutex>
 
 #include <cuda.h>
@@ -36,7 +37,7 @@ TimingEvents timing_events() {
   std::lock_guard<std::mutex> lk(g_timing_mu);
   return g_timing;
 }
-constexpr unsigned long long kDefaultWaitLimitNs = 2000ull * 1000 * 1000;
+constexpr unsigned long long kDefaultWaitLimitNs = 10000ull * 1000 * 1000;
 
 unsigned long long wait_limit_ns() {
   const unsigned long long v = g_wait_limit_ns.load(std::memory_order_relaxed);
@@ -87,13 +88,41 @@ bool encode_u8_3d(CUtensorMap* map, const void* ptr, int inner, int rows, long l
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// shape checks shared by every entry point
+// shape checks shared by every entry point.  Sizes arrive as int; the
+// kernels address memory with 64-bit offsets and count their work items
+// (128-row blocks of every (batch, head), and the forward's pairs of them) in
+// int, so B * H and (ceil(N / 128) + 1) * B * H must stay below 2^31.  That
+// bounds B * H * N * d by 2^45 elements, far beyond the device's memory.
 fa_status check_shape(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const long long bh = (long long)B * H;
-  if (bh > 65535LL * 65535LL) return FA_ERR_INVALID_ARG;
-  if (bh * N * d >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+  if (bh > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  const long long blocks = ((long long)N + 127) / 128;
+  if ((blocks + 1) * bh > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+// Every tensor argument must be memory the current device's kernels can read
+// and write: device memory of the current device, or managed memory.  Host
+// memory, another device's memory and addresses no allocation covers are
+// refused before anything is enqueued (a kernel given one would fault).
+fa_status check_device_ptrs(std::initializer_list<const void*> ptrs) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  for (const void* ptr : ptrs) {
+    cudaPointerAttributes a{};
+    const cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+    if (e != cudaSuccess) {
+      cudaGetLastError();  // leave no error behind for the launch checks that follow
+      return e == cudaErrorInvalidValue ? FA_ERR_INVALID_ARG : FA_ERR_CUDA;
+    }
+    if (a.type == cudaMemoryTypeManaged) continue;
+    if (a.type != cudaMemoryTypeDevice || a.device != dev) return FA_ERR_INVALID_ARG;
+  }
   return FA_OK;
 }
 
@@ -402,6 +431,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   if (st != FA_OK) return st;
   if ((st = check_scale(scale, causal)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
+  if ((st = check_device_ptrs({q, k, v, o, lse})) != FA_OK) return st;
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
   if (!encode_bhnd(&mq, q, BH, N, d) || !encode_bhnd(&mk, k, BH, N, d) || !encode_bhnd(&mv, v, BH, N, d))
@@ -435,6 +465,9 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, const signed c
   if (ws_bytes < fa_fwd_fp8_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
     return FA_ERR_MISALIGNED;
+  // the operand preparation's grid has one y index per (batch, head)
+  if ((long long)B * H > 65535) return FA_ERR_UNSUPPORTED;
+  if ((st = check_device_ptrs({q, k, v, signs, o, lse, workspace})) != FA_OK) return st;
   const int BH = B * H;
   const int nkb = (N + 127) / 128;
   const Fp8Workspace w = Fp8Workspace::of(B, H, N);
@@ -490,6 +523,7 @@ fa_status fa_bwd_preprocess(const void* o, const void* dout, float* delta, int B
   fa_status st = check_shape(B, H, N, d);
   if (st != FA_OK) return st;
   if (!aligned16(o) || !aligned16(dout) || !aligned16(delta)) return FA_ERR_MISALIGNED;
+  if ((st = check_device_ptrs({o, dout, delta})) != FA_OK) return st;
   return launch_preprocess(o, dout, delta, nullptr, (long long)B * H * N, d, stream);
 }
 
@@ -504,6 +538,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
     return FA_ERR_MISALIGNED;
+  if ((st = check_device_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace})) != FA_OK) return st;
   return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, H, N, d, scale, causal, false, stream);
 }
 
@@ -518,6 +553,7 @@ fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, cons
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
     return FA_ERR_MISALIGNED;
+  if ((st = check_device_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace})) != FA_OK) return st;
   return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, H, N, d, scale, causal, true, stream);
 }
 
@@ -576,6 +612,7 @@ fa_status fa_bwd_static_scratch(const void* q, const void* k, const void* v, con
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_MISALIGNED;
+  if ((st = check_device_ptrs({q, k, v, o, dout, lse, dq, dk, dv})) != FA_OK) return st;
   void* scratch = nullptr;
   if ((st = static_scratch_on_current_device(&scratch)) != FA_OK) return st;
   // the previous call's contents stay in the array: the preprocess rewrites

@@ -10,6 +10,7 @@ If the compiled library is missing, loading fails loudly.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -84,12 +85,22 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     return lib
 
 
-def _stream_handle(stream) -> int:
+def _stream_handle(stream, device=None) -> int:
+    """The raw handle of ``stream``: None is the current stream of ``device``
+    (or of the current device); a torch stream must live on ``device``."""
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        return torch.cuda.current_stream(device).cuda_stream
     if isinstance(stream, torch.cuda.Stream):
+        if device is not None and stream.device != device:
+            raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
         return stream.cuda_stream
     return int(stream)
+
+
+def _on_device(device: torch.device):
+    """The library launches on the current device, so each call makes the
+    tensors' device current for its duration."""
+    return torch.cuda.device(device) if device.type == "cuda" else contextlib.nullcontext()
 
 
 def _shape4(t: torch.Tensor, name: str):
@@ -107,6 +118,8 @@ def _check(t: torch.Tensor, name: str, dtype, shape, device):
         raise ValueError(f"{name} must be contiguous")
     if t.device != device:
         raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor, got one on {t.device}")
 
 
 def _raise(status: int, where: str):
@@ -144,8 +157,11 @@ def fa_set_timing_events(fwd_start=None, fwd_stop=None, bwd_start=None, bwd_stop
 
 
 def fa_check_device_status(stream=None) -> int:
-    """Synchronize the stream; return (and clear) the device status word."""
-    return int(load_library().fa_check_device_status(_stream_handle(stream)))
+    """Synchronize the stream; return (and clear) the status word of the
+    stream's device (of the current device for None or a raw handle)."""
+    dev = stream.device if isinstance(stream, torch.cuda.Stream) else None
+    with (torch.cuda.device(dev) if dev is not None else contextlib.nullcontext()):
+        return int(load_library().fa_check_device_status(_stream_handle(stream)))
 
 
 def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None) -> None:
@@ -155,8 +171,9 @@ def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None) -> None:
     for t, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
         _check(t, name, torch.bfloat16, (B, H, N, d), dev)
     _check(lse, "lse", torch.float32, (B, H, N), dev)
-    st = load_library().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                               B, H, N, d, float(scale), int(bool(causal)), _stream_handle(stream))
+    with _on_device(dev):
+        st = load_library().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                   B, H, N, d, float(scale), int(bool(causal)), _stream_handle(stream, dev))
     _raise(st, "fa_fwd")
 
 
@@ -177,9 +194,10 @@ def fa_fwd_fp8(q, k, v, signs, o, lse, workspace, scale: float, causal: bool, st
     if workspace.device != dev or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous tensor on the inputs' device")
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = load_library().fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), signs.data_ptr(), o.data_ptr(),
-                                   lse.data_ptr(), workspace.data_ptr(), ws_bytes, B, H, N, d, float(scale),
-                                   int(bool(causal)), _stream_handle(stream))
+    with _on_device(dev):
+        st = load_library().fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), signs.data_ptr(), o.data_ptr(),
+                                       lse.data_ptr(), workspace.data_ptr(), ws_bytes, B, H, N, d, float(scale),
+                                       int(bool(causal)), _stream_handle(stream, dev))
     _raise(st, "fa_fwd_fp8")
 
 
@@ -190,8 +208,9 @@ def fa_bwd_preprocess(o, dout, delta, stream=None) -> None:
     _check(o, "o", torch.bfloat16, (B, H, N, d), dev)
     _check(dout, "dout", torch.bfloat16, (B, H, N, d), dev)
     _check(delta, "delta", torch.float32, (B, H, N), dev)
-    st = load_library().fa_bwd_preprocess(o.data_ptr(), dout.data_ptr(), delta.data_ptr(), B, H, N, d,
-                                          _stream_handle(stream))
+    with _on_device(dev):
+        st = load_library().fa_bwd_preprocess(o.data_ptr(), dout.data_ptr(), delta.data_ptr(), B, H, N, d,
+                                              _stream_handle(stream, dev))
     _raise(st, "fa_bwd_preprocess")
 
 
@@ -208,10 +227,11 @@ def _bwd_call(entry: str, q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: f
     if workspace.device != dev or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous tensor on the inputs' device")
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = getattr(load_library(), entry)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
-                                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                                        workspace.data_ptr(), ws_bytes, B, H, N, d, float(scale),
-                                        int(bool(causal)), _stream_handle(stream))
+    with _on_device(dev):
+        st = getattr(load_library(), entry)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                            dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                            dv.data_ptr(), workspace.data_ptr(), ws_bytes, B, H, N, d, float(scale),
+                                            int(bool(causal)), _stream_handle(stream, dev))
     _raise(st, entry)
 
 
@@ -239,39 +259,58 @@ def fa_bwd_static_scratch(q, k, v, o, dout, lse, dq, dk, dv, scale: float, causa
     for t, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
         _check(t, name, torch.bfloat16, (B, H, N, d), dev)
     _check(lse, "lse", torch.float32, (B, H, N), dev)
-    st = load_library().fa_bwd_static_scratch(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
-                                              lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                                              B, H, N, d, float(scale), int(bool(causal)), _stream_handle(stream))
+    with _on_device(dev):
+        st = load_library().fa_bwd_static_scratch(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                                  dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                                  dv.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
+                                                  _stream_handle(stream, dev))
     _raise(st, "fa_bwd_static_scratch")
 
 
 # ---------------------------------------------------------------------------
-# conveniences that allocate the outputs with torch and call the entry points
+# conveniences that allocate the outputs with torch and call the entry points.
+# With check_status (the default) they wait for the work and raise FaError if
+# a kernel reported a timeout, so what they return is known to be valid; pass
+# check_status=False to keep the call asynchronous and check later with
+# fa_check_device_status.
 # ---------------------------------------------------------------------------
-def attention_forward(q, k, v, scale: float, causal: bool = False, stream=None):
+def _checked(stream, device, where: str):
+    with _on_device(device):
+        st = int(load_library().fa_check_device_status(_stream_handle(stream, device)))
+    _raise(st, where)
+
+
+def attention_forward(q, k, v, scale: float, causal: bool = False, stream=None, check_status: bool = True):
     B, H, N, d = _shape4(q, "q")
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, o, lse, scale, causal, stream)
+    if check_status:
+        _checked(stream, q.device, "attention_forward")
     return o, lse
 
 
-def attention_forward_fp8(q, k, v, signs, scale: float, causal: bool = False, workspace=None, stream=None):
+def attention_forward_fp8(q, k, v, signs, scale: float, causal: bool = False, workspace=None, stream=None,
+                          check_status: bool = True):
     B, H, N, d = _shape4(q, "q")
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = torch.empty(fa_fwd_fp8_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
     fa_fwd_fp8(q, k, v, signs, o, lse, workspace, scale, causal, stream)
+    if check_status:
+        _checked(stream, q.device, "attention_forward_fp8")
     return o, lse
 
 
 def attention_backward(q, k, v, o, dout, lse, scale: float, causal: bool = False, workspace=None, stream=None,
-                       deterministic: bool = False):
+                       deterministic: bool = False, check_status: bool = True):
     B, H, N, d = _shape4(q, "q")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
         workspace = torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
     (fa_bwd_deterministic if deterministic else fa_bwd)(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal,
                                                         stream)
+    if check_status:
+        _checked(stream, q.device, "attention_backward")
     return dq, dk, dv

@@ -33,13 +33,30 @@
  * Streams.  Calls only enqueue work on `stream` (0 = legacy default stream) and
  *   return the launch status; they do not synchronize.  A device-side timeout
  *   is reported later by fa_check_device_status.
+ * Device.  Every call runs on the CURRENT device (cudaGetDevice): the caller
+ *   makes the tensors' device current first.  Every tensor pointer must be
+ *   device memory of that device, or managed memory; anything else (host
+ *   memory, another device's memory, an address no allocation covers) gives
+ *   FA_ERR_INVALID_ARG before anything is enqueued.
  * Errors.  Arguments are validated before anything is enqueued; on an error
- *   nothing runs and no output is written.  Invalid sizes, a null pointer or
- *   a non-finite / non-positive scale give FA_ERR_INVALID_ARG; a pointer not
- *   on a 16-byte boundary gives FA_ERR_MISALIGNED; a head dimension other
- *   than 64 or 128 gives FA_ERR_UNSUPPORTED; a failed CUDA call (including a
- *   device without sm_103a support) gives FA_ERR_CUDA.
- * Limits.  1 <= B, H, N; B * H * N * d < 2^31; B * H <= 65535 * 65535.
+ *   nothing runs and no output is written.  Invalid sizes, a null pointer, a
+ *   pointer the current device cannot use (above) or a non-finite /
+ *   non-positive scale give FA_ERR_INVALID_ARG; a pointer not on a 16-byte
+ *   boundary gives FA_ERR_MISALIGNED; a head dimension other than 64 or 128
+ *   gives FA_ERR_UNSUPPORTED; a failed CUDA call (including a device without
+ *   sm_103a support) gives FA_ERR_CUDA.
+ * Validity of the outputs.  A returned FA_OK means the work was enqueued.
+ *   Every wait inside the kernels is bounded in time (fa_set_wait_limit_ns,
+ *   default 10 s); a kernel whose wait runs out -- which also happens if the
+ *   GPU stops running it for longer than the limit, e.g. under heavy time
+ *   slicing -- stops early, leaves its outputs undefined and records
+ *   FA_ERR_TIMEOUT in the device status word.  The outputs of a sequence of
+ *   calls are therefore known to be valid only once fa_check_device_status
+ *   has returned FA_OK after them.
+ * Limits.  1 <= B, H, N; B * H < 2^31 and (ceil(N / 128) + 1) * B * H < 2^31
+ *   (the kernels count 128-row blocks in 32-bit integers and address memory
+ *   with 64-bit offsets, so B * H * N * d itself may exceed 2^31);
+ *   fa_fwd_fp8 also needs B * H <= 65535.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -193,8 +210,11 @@ fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, cons
  * FA_STATIC_SCRATCH_BYTES (72 MiB; roughly B*H*N*(d+2)*4 bytes must fit, as
  * for B=4, H=16, N=2048, d=128) return FA_ERR_INVALID_ARG and run nothing.
  * Set-up: the first call on a device looks up the array's device address on
- * that device (cudaGetSymbolAddress, with that device current) and caches it;
- * make that first call outside any stream capture.  Sharing: every call uses
+ * that device (cudaGetSymbolAddress, with that device current) and caches it
+ * for the life of the process; make that first call outside any stream
+ * capture.  The cached address belongs to the device's context: after
+ * cudaDeviceReset (which destroys that context and the array with it) this
+ * entry point must not be called again in the same process.  Sharing: every call uses
  * the same array and the array keeps the last call's contents (each call
  * re-initialises what it reads).  Calls whose work overlaps on the GPU (on
  * different streams, or from different threads) race on the array and give
@@ -215,7 +235,7 @@ fa_status fa_check_device_status(cudaStream_t stream);
 
 /*
  * Upper bound, in nanoseconds, on every barrier wait inside the kernels
- * launched after this call (process-wide; 0 restores the default of two
+ * launched after this call (process-wide; 0 restores the default of ten
  * seconds).  A wait that runs out makes the kernel stop early and report
  * FA_ERR_TIMEOUT through fa_check_device_status; it never traps.  Meant for
  * tests of that path.

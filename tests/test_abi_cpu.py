@@ -65,8 +65,9 @@ def test_fwd_validation(lib):
     assert fwd(lib, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
     assert fwd(lib, scale=float("inf")) == fa.FA_ERR_INVALID_ARG
     assert fwd(lib, causal=2) == fa.FA_ERR_INVALID_ARG
-    assert fwd(lib, B=1 << 16, H=1 << 16) == fa.FA_ERR_INVALID_ARG   # B*H*N*d overflows
-    assert fwd(lib, N=1 << 24) == fa.FA_ERR_INVALID_ARG              # B*H*N*d >= 2^31
+    assert fwd(lib, B=1 << 16, H=1 << 15) == fa.FA_ERR_INVALID_ARG   # B*H = 2^31
+    assert fwd(lib, B=1 << 15, H=1 << 15, N=1 << 20) == fa.FA_ERR_INVALID_ARG  # 128-row blocks x B*H >= 2^31
+    assert fwd(lib, B=1 << 10, H=1 << 8, N=1 << 14, q=BAD) == fa.FA_ERR_MISALIGNED  # 2^39 elements: shape accepted
     assert fwd(lib, q=BAD) == fa.FA_ERR_MISALIGNED
     assert fwd(lib, o=BAD) == fa.FA_ERR_MISALIGNED
     assert fwd(lib, lse=P + 4) == fa.FA_ERR_MISALIGNED
@@ -139,4 +140,21 @@ def test_fwd_fp8_validation(lib):
     assert call(d=64) == fa.FA_ERR_UNSUPPORTED
     assert call(scale=-1.0) == fa.FA_ERR_INVALID_ARG
     assert call(ws=BAD) == fa.FA_ERR_MISALIGNED
+
+
+def test_fwd_fp8_rejects_more_than_65535_heads(lib):
+    # the operand preparation's grid has one y index per (batch, head)
+    B, H, N = 256, 257, 128
+    need = lib.fa_fwd_fp8_workspace_bytes(B, H, N, 128)
+    assert need > 0
+    assert lib.fa_fwd_fp8(VP(P), VP(P), VP(P), VP(P), VP(P), VP(P), VP(P), need, B, H, N, 128, 0.1, 0,
+                          None) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_workspace_bytes_past_2_31_elements(lib):
+    # B*H*N*d above 2^31 is accepted; sizes are computed in 64 bits
+    B, H, N, d = 1, 8193, 2048, 128
+    rows = B * H * N
+    assert rows * d > 1 << 31
+    assert lib.fa_bwd_workspace_bytes(B, H, N, d) == (rows * d * 4 + 255) // 256 * 256 + 2 * ((rows * 4 + 255) // 256 * 256)
 

@@ -1,8 +1,9 @@
 """The bounded waits: with the debug stall on, each kernel's MMA thread waits
 on a barrier that nothing signals; after the (short) wait limit the kernel
 reports FA_ERR_TIMEOUT through the status word, drains the copies it started
-and returns.  The context stays usable and the next call, with the stall off
-and the default limit, is correct.  Nothing here traps or hangs."""
+and returns; the checking conveniences raise it as FaError.  The context
+stays usable and the next call, with the stall off and the default limit, is
+correct.  Nothing here traps or hangs."""
 
 import math
 
@@ -35,9 +36,15 @@ def test_forward_wait_timeout_is_reported_and_recoverable():
     assert fa.fa_check_device_status() == fa.FA_OK
     fa.fa_set_wait_limit_ns(1_000_000)  # 1 ms
     fa.fa_debug_stall(True)
-    fa.attention_forward(q, k, v, scale, False)
+    # asynchronous form: the call returns FA_OK, the status word holds the timeout
+    fa.attention_forward(q, k, v, scale, False, check_status=False)
     assert fa.fa_check_device_status() == fa.FA_ERR_TIMEOUT
     assert fa.fa_check_device_status() == fa.FA_OK  # cleared by the read
+    # checked form (the conveniences' default): the timeout is raised
+    with pytest.raises(fa.FaError) as err:
+        fa.attention_forward(q, k, v, scale, False)
+    assert err.value.status == fa.FA_ERR_TIMEOUT
+    assert fa.fa_check_device_status() == fa.FA_OK
     fa.fa_debug_stall(False)
     fa.fa_set_wait_limit_ns(0)
     o, lse = fa.attention_forward(q, k, v, scale, False)
@@ -55,8 +62,10 @@ def test_backward_wait_timeout_is_reported_and_recoverable():
     assert fa.fa_check_device_status() == fa.FA_OK
     fa.fa_set_wait_limit_ns(1_000_000)
     fa.fa_debug_stall(True)
-    fa.attention_backward(q, k, v, o, do, lse, scale, True)
-    assert fa.fa_check_device_status() == fa.FA_ERR_TIMEOUT
+    with pytest.raises(fa.FaError) as err:
+        fa.attention_backward(q, k, v, o, do, lse, scale, True)
+    assert err.value.status == fa.FA_ERR_TIMEOUT
+    assert fa.fa_check_device_status() == fa.FA_OK
     fa.fa_debug_stall(False)
     fa.fa_set_wait_limit_ns(0)
     dq, dk, dv = fa.attention_backward(q, k, v, o, do, lse, scale, True)
