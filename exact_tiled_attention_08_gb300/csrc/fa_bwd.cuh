@@ -227,6 +227,7 @@ struct BwdParams {
   float scale;
   uint64_t wait_limit_ns;
   int debug_stall;  // nonzero: issuer A first waits on `never` (tests the timeout path)
+  int out_align32;  // nonzero: dk_out and dv_out are 32-byte aligned (32-byte stores)
 };
 
 // The CTA's items: blockIdx.x, blockIdx.x + gridDim.x, ...
@@ -715,15 +716,19 @@ __global__ void __launch_bounds__(512, 1)
           tmem_wait_ld();
           reg_fence32(v);
           if (kg < N) {
-            uint4* o4 = reinterpret_cast<uint4*>(out + 32 * c);
+            uint32_t w16[16];
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint4 w4;
-              w4.x = pack_bf16x2(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
-              w4.y = pack_bf16x2(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
-              w4.z = pack_bf16x2(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
-              w4.w = pack_bf16x2(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
-              o4[v4] = w4;
+            for (int e = 0; e < 16; ++e)
+              w16[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+            if (p.out_align32) {
+              // whole 32-byte sectors (a thread's row is contiguous)
+              st_global_v8(out + 32 * c, w16);
+              st_global_v8(out + 32 * c + 16, w16 + 8);
+            } else {
+              uint4* o4 = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                o4[v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2], w16[4 * v4 + 3]);
             }
           }
         }

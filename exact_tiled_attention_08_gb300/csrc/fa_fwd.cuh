@@ -56,6 +56,28 @@ constexpr float kRescaleThresholdLog2 = 8.0f;
 
 constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;  // waits while draining after an abort
 
+// 2^x on the FMA pipe, the software exponential of "Interrogating the GPU
+// part 5: FlashAttention", "Why did Blackwell need FlashAttention-4?":
+// 2^x = 2^n 2^f with n = floor(x), f = x - n in [0, 1), and 2^f taken as the
+// cubic 1 + 0.6951 f + 0.2276 f^2 + 0.0771 f^3 (relative error <= 1.0e-4,
+// largest as f -> 1; a bf16 probability's rounding is 2^-9).  floor(x) comes
+// from adding 1.5 * 2^23 rounded toward -inf, which leaves it as the integer
+// in the low mantissa bits; 2^n is applied by adding n to the exponent field.
+// x is clamped below at -127: x = -127 (and -inf) gives exactly 0, x in
+// (-127, -126) a value below 2^-126 that the flush-to-zero arithmetic
+// downstream treats as 0.  Arguments here never exceed the rescale threshold
+// (8), far from the upper end of the exponent range.
+__device__ __forceinline__ float ex2_cubic(float x) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  x = fmaxf(x, -127.f);
+  const float t = __fadd_rd(x, kMagic);
+  const float f = x - (t - kMagic);  // both subtractions exact: f = x - floor(x)
+  float p = fmaf(f, 0.0771f, 0.2276f);
+  p = fmaf(p, f, 0.6951f);
+  p = fmaf(p, f, 1.f);
+  return __uint_as_float(__float_as_uint(p) + ((__float_as_uint(t) - __float_as_uint(kMagic)) << 23));
+}
+
 // FP8: the E4M3 variant of the same kernel (fa_fwd_fp8): Q and K arrive
 // rotated and quantised per 128-row block, V quantised per channel and stored
 // transposed per key block (d rows of 128 keys, K-major), P is rounded to E4M3
@@ -132,6 +154,7 @@ struct FwdParams {
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
   int debug_stall;  // nonzero: the MMA thread first waits on `never` (tests the timeout path)
+  int o_align32;    // nonzero: o is 32-byte aligned, so O rows are written in 32-byte stores
   // FP8 only: dequantisation scales
   const float* q_scale;  // [B*H][nkb]: query block scales
   const float* k_scale;  // [B*H][nkb]: key block scales
@@ -193,7 +216,10 @@ __device__ __forceinline__ bool fwd_item(const FwdParams& p, int k, FwdItem& w) 
   return true;
 }
 
-template <int D, bool CAUSAL, bool FP8 = false>
+// SOFT_EXP: of every four pairs of probabilities a softmax thread forms, the
+// first SOFT_EXP pairs take ex2_cubic on the FMA pipe and the rest the MUFU's
+// ex2.approx (0: all on the MUFU).
+template <int D, bool CAUSAL, bool FP8 = false, int SOFT_EXP = 0>
 __global__ void __launch_bounds__(352, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
@@ -530,8 +556,14 @@ __global__ void __launch_bounds__(352, 1)
           for (int i = 0; i < 16; ++i) {
             const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
                                         c2, mneg2);
-            const float p0 = ex2_approx(x.x);
-            const float p1 = ex2_approx(x.y);
+            float p0, p1;
+            if (SOFT_EXP > 0 && (i & 3) < SOFT_EXP) {
+              p0 = ex2_cubic(x.x);
+              p1 = ex2_cubic(x.y);
+            } else {
+              p0 = ex2_approx(x.x);
+              p1 = ex2_approx(x.y);
+            }
             if constexpr (FP8) {
               if (i & 1) {
                 pk[c][i >> 1] = pack_e4m3x4(hold0, hold1, p0, p1);
@@ -636,15 +668,19 @@ __global__ void __launch_bounds__(352, 1)
           }
         }
         if (row_g < N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+          uint32_t w16[16];
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 q4;
-            q4.x = pack_bf16x2(__uint_as_float(ov[8 * v4 + 0]) * inv_l, __uint_as_float(ov[8 * v4 + 1]) * inv_l);
-            q4.y = pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * inv_l, __uint_as_float(ov[8 * v4 + 3]) * inv_l);
-            q4.z = pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * inv_l, __uint_as_float(ov[8 * v4 + 5]) * inv_l);
-            q4.w = pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * inv_l, __uint_as_float(ov[8 * v4 + 7]) * inv_l);
-            dst[v4] = q4;
+          for (int e = 0; e < 16; ++e)
+            w16[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+          if (p.o_align32) {
+            // whole 32-byte sectors (a thread's row is contiguous)
+            st_global_v8(orow + 32 * c, w16);
+            st_global_v8(orow + 32 * c + 16, w16 + 8);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2], w16[4 * v4 + 3]);
           }
         }
       }

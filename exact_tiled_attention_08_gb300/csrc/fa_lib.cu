@@ -25,6 +25,7 @@ namespace {
 
 std::atomic<unsigned long long> g_wait_limit_ns{0};
 std::atomic<int> g_debug_stall{0};
+std::atomic<int> g_exp2_soft_quarters{0};
 
 // caller-owned events recorded around the main kernels (profiling hook)
 struct TimingEvents {
@@ -87,6 +88,7 @@ bool encode_u8_3d(CUtensorMap* map, const void* ptr, int inner, int rows, long l
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // shape checks shared by every entry point.  Sizes arrive as int; the
 // kernels address memory with 64-bit offsets and count their work items
@@ -137,11 +139,11 @@ cudaError_t set_smem(Kernel kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int D, bool CAUSAL, bool FP8 = false>
+template <int D, bool CAUSAL, bool FP8 = false, int SOFT_EXP = 0>
 fa_status launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, fa::FwdParams p,
                      int BH, cudaStream_t stream) {
   using C = fa::FwdCfg<D, FP8>;
-  auto kernel = fa::fa_fwd_kernel<D, CAUSAL, FP8>;
+  auto kernel = fa::fa_fwd_kernel<D, CAUSAL, FP8, SOFT_EXP>;
   if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
   // persistent CTAs: one per SM (the kernel holds a whole SM), never more than there are items
   int dev = 0, sms = 0;
@@ -335,6 +337,7 @@ fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, co
   p.scale = scale;
   p.wait_limit_ns = wait_limit_ns();
   p.debug_stall = g_debug_stall.load();
+  p.out_align32 = aligned32(dk) && aligned32(dv);
   fa_status st;
   if (deterministic) {
     if (d == 128)
@@ -404,6 +407,12 @@ void fa_set_wait_limit_ns(unsigned long long limit_ns) { g_wait_limit_ns.store(l
 
 void fa_debug_stall(int enable) { g_debug_stall.store(enable ? 1 : 0); }
 
+fa_status fa_set_exp2_split(int soft_quarters) {
+  if (soft_quarters < 0 || soft_quarters > 2) return FA_ERR_INVALID_ARG;
+  g_exp2_soft_quarters.store(soft_quarters);
+  return FA_OK;
+}
+
 void fa_set_timing_events(cudaEvent_t fwd_start, cudaEvent_t fwd_stop, cudaEvent_t bwd_start, cudaEvent_t bwd_stop) {
   std::lock_guard<std::mutex> lk(g_timing_mu);
   g_timing.fwd_start = fwd_start;
@@ -438,6 +447,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     return FA_ERR_CUDA;
   fa::FwdParams p{};
   p.o = static_cast<__nv_bfloat16*>(o);
+  p.o_align32 = aligned32(o);
   p.lse = lse;
   p.N = N;
   p.num_pairs = (N + 255) / 256;
@@ -445,8 +455,24 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = wait_limit_ns();
   p.debug_stall = g_debug_stall.load();
-  if (d == 128) return causal ? launch_fwd<128, true>(mq, mk, mv, p, BH, stream) : launch_fwd<128, false>(mq, mk, mv, p, BH, stream);
-  return causal ? launch_fwd<64, true>(mq, mk, mv, p, BH, stream) : launch_fwd<64, false>(mq, mk, mv, p, BH, stream);
+  switch (g_exp2_soft_quarters.load()) {
+    case 1:
+      if (d == 128)
+        return causal ? launch_fwd<128, true, false, 1>(mq, mk, mv, p, BH, stream)
+                      : launch_fwd<128, false, false, 1>(mq, mk, mv, p, BH, stream);
+      return causal ? launch_fwd<64, true, false, 1>(mq, mk, mv, p, BH, stream)
+                    : launch_fwd<64, false, false, 1>(mq, mk, mv, p, BH, stream);
+    case 2:
+      if (d == 128)
+        return causal ? launch_fwd<128, true, false, 2>(mq, mk, mv, p, BH, stream)
+                      : launch_fwd<128, false, false, 2>(mq, mk, mv, p, BH, stream);
+      return causal ? launch_fwd<64, true, false, 2>(mq, mk, mv, p, BH, stream)
+                    : launch_fwd<64, false, false, 2>(mq, mk, mv, p, BH, stream);
+    default:
+      if (d == 128)
+        return causal ? launch_fwd<128, true>(mq, mk, mv, p, BH, stream) : launch_fwd<128, false>(mq, mk, mv, p, BH, stream);
+      return causal ? launch_fwd<64, true>(mq, mk, mv, p, BH, stream) : launch_fwd<64, false>(mq, mk, mv, p, BH, stream);
+  }
 }
 
 size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d) {
@@ -497,6 +523,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, const signed c
     return FA_ERR_CUDA;
   fa::FwdParams p{};
   p.o = static_cast<__nv_bfloat16*>(o);
+  p.o_align32 = aligned32(o);
   p.lse = lse;
   p.N = N;
   p.num_pairs = (N + 255) / 256;

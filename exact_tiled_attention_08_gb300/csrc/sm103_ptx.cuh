@@ -419,6 +419,14 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, fl
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// 32-byte store of eight 32-bit words (the address must be 32-byte aligned):
+// a whole sector per thread, where a 16-byte store would write half of one
+__device__ __forceinline__ void st_global_v8(void* gptr, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(gptr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // fp32 vector reduction into global memory (no return value)
 __device__ __forceinline__ void red_add_v4(float* gptr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gptr), "f"(a), "f"(b), "f"(c), "f"(d)

@@ -76,6 +76,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_set_wait_limit_ns.restype = None
     lib.fa_debug_stall.argtypes = [i]
     lib.fa_debug_stall.restype = None
+    lib.fa_set_exp2_split.argtypes = [i]
+    lib.fa_set_exp2_split.restype = i
     lib.fa_set_timing_events.argtypes = [vp, vp, vp, vp]
     lib.fa_set_timing_events.restype = None
     lib.fa_status_string.argtypes = [i]
@@ -138,6 +140,12 @@ def fa_set_wait_limit_ns(limit_ns: int) -> None:
 def fa_debug_stall(enable: bool) -> None:
     """Test hook: kernels launched while enabled stall on a barrier nothing signals."""
     load_library().fa_debug_stall(int(bool(enable)))
+
+
+def fa_set_exp2_split(soft_quarters: int) -> None:
+    """0 (default): every forward exponential on the special-function unit;
+    1 or 2: that many of every four pairs by the cubic 2^n p(f) on the FMA pipe."""
+    _raise(load_library().fa_set_exp2_split(int(soft_quarters)), "fa_set_exp2_split")
 
 
 def _event_handle(ev) -> int:

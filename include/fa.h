@@ -253,6 +253,22 @@ void fa_set_wait_limit_ns(unsigned long long limit_ns);
 void fa_debug_stall(int enable);
 
 /*
+ * Where fa_fwd evaluates its exponentials ("Interrogating the GPU part 5:
+ * FlashAttention", section "Why did Blackwell need FlashAttention-4?": part of
+ * the exponentials run in software as 2^n times a cubic in the fraction, on
+ * the FMA units, the rest on the special-function unit).  soft_quarters = 0
+ * (the default) computes every probability with the special-function unit's
+ * ex2; 1 or 2 computes that many of every four pairs of probabilities a
+ * softmax thread forms with the cubic 1 + 0.6951 f + 0.2276 f^2 + 0.0771 f^3
+ * (relative error <= 1.0e-4, 20 times below a bf16 probability's rounding).
+ * The results stay within the same tolerances; only the speed differs.
+ * Applies to the bf16 forward launched after the call (fa_fwd_fp8 always uses
+ * the special-function unit).  Process-wide.  Other values give
+ * FA_ERR_INVALID_ARG and change nothing.
+ */
+fa_status fa_set_exp2_split(int soft_quarters);
+
+/*
  * Profiling hook.  While set, fa_fwd and fa_fwd_fp8 record fwd_start and
  * fwd_stop on their stream immediately before and after launching the
  * attention kernel (not around fa_fwd_fp8's operand preparation), and fa_bwd

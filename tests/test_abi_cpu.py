@@ -26,13 +26,20 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_workspace_bytes", "fa_check_device_status",
-                     "fa_status_string", "fa_set_wait_limit_ns", "fa_debug_stall", "fa_set_timing_events"):
+                     "fa_status_string", "fa_set_wait_limit_ns", "fa_debug_stall", "fa_set_timing_events",
+                     "fa_set_exp2_split"):
         assert required in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
+
+
+def test_exp2_split_validation(lib):
+    assert lib.fa_set_exp2_split(3) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_set_exp2_split(-1) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_set_exp2_split(0) == fa.FA_OK
 
 
 def test_status_strings(lib):

@@ -147,3 +147,28 @@ def test_forward_full_size_workloads(name):
     q0 = inp["q"][:, :, 0, :].float().cuda()
     k0 = inp["k"][:, :, 0, :].float().cuda()
     assert (lse[:, :, 0] >= (q0 * k0).sum(-1) * w.scale - LSE_TOL).all()
+
+
+@pytest.mark.parametrize("soft_quarters", [1, 2])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_forward_with_software_exp2(soft_quarters, causal, d):
+    """Part of the exponentials by the pages' cubic 2^n p(f) on the FMA pipe
+    (fa_set_exp2_split): same tolerances.  Ragged N, the rescale-stress keys
+    (arguments far below 0 and up to the rescale threshold) and a masked
+    diagonal all pass through the software path."""
+    inp = make_inputs(2, 2, 777, d, seed=300 + d + soft_quarters, key_outliers=True)
+    scale = 1.0 / math.sqrt(d)
+    fa.fa_set_exp2_split(soft_quarters)
+    try:
+        o, lse = gpu_forward(inp, scale, causal)
+    finally:
+        fa.fa_set_exp2_split(0)
+    check_heads(inp, o, lse, scale, causal)
+
+
+def test_exp2_split_rejects_other_values():
+    with pytest.raises(fa.FaError):
+        fa.fa_set_exp2_split(3)
+    with pytest.raises(fa.FaError):
+        fa.fa_set_exp2_split(-1)
