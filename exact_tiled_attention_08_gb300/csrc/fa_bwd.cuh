@@ -214,6 +214,8 @@ struct BwdBarriers {
   int abort_flag;
 };
 
+static_assert(sizeof(BwdBarriers) <= 256, "barriers overflow their shared-memory slot");
+
 struct BwdParams {
   float* dq_acc;  // [B*H][N][d] fp32, zeroed by the preprocess
   __nv_bfloat16* dk_out;

@@ -63,6 +63,8 @@ struct BwdDqBarriers {
   int abort_flag;
 };
 
+static_assert(sizeof(BwdDqBarriers) <= 256, "barriers overflow their shared-memory slot");
+
 struct BwdDqParams {
   const float* delta_pad;  // [B*H][Npad] delta, 0 past N
   const float* lse2_pad;   // [B*H][Npad] LSE * log2(e), +inf past N

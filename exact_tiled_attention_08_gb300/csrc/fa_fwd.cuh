@@ -143,6 +143,8 @@ struct FwdBarriers {
   int abort_flag;
 };
 
+static_assert(sizeof(FwdBarriers) <= 512, "barriers overflow their shared-memory slot");
+
 struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
