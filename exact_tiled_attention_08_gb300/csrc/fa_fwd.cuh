@@ -103,6 +103,11 @@ struct FwdCfg {
   static constexpr bool kSumByMma = FP8;
   static constexpr int kOCols = kSumByMma ? D + 16 : D;  // O accumulator columns
   static constexpr int kOnesBytes = FP8 ? 16 * 128 : 0;
+  // bf16 d = 128: O is normalised by the fp32 sum plus the rounding error of
+  // each key block's largest probability (see the softmax); bf16 d = 64, where
+  // the cheaper form gains nothing and raises register use, by the sum of the
+  // rounded probabilities themselves
+  static constexpr bool kBlockMaxCorr = !FP8 && D == 128;
   // bf16 d = 64: a score buffer per tile (S_0 first, S_1 after the O
   // accumulators: 128 + 2 x 64 + 2 x 64 + 128 = 512 columns), so that a tile's
   // next scores never wait for the other tile to load its own.  At d = 128
@@ -477,7 +482,11 @@ __global__ void __launch_bounds__(352, 1)
       // FP8: the scores are the E4M3 products times the query and key block scales
       const float qsl2 = FP8 ? sl2 * __ldg(p.q_scale + (size_t)w.bh * p.nkb + (row_q0 >> 7)) : sl2;
       float m = -CUDART_INF_F;  // exponent reference (log2 units), a stale running max
-      float l = 0.f, l_mma = 0.f;
+      // l: sum of the fp32 probabilities (for the LSE); lcorr (bf16, d = 128):
+      // the rounding errors of each key block's largest probability, so that
+      // l + lcorr normalises O (below); l_mma: the sum of the rounded
+      // probabilities (bf16 d = 64; FP8: formed by the tensor core)
+      float l = 0.f, lcorr = 0.f, l_mma = 0.f;
       for (int j = 0; j < nb; ++j, ++uses) {
         // score factor of this key block (loaded before the wait hides its latency)
         const float cj = FP8 ? qsl2 * __ldg(p.k_scale + (size_t)w.bh * p.nkb + j) : sl2;
@@ -539,15 +548,25 @@ __global__ void __launch_bounds__(352, 1)
             m = m_new;
           }
         }
-        // p = 2^(s c - m) two at a time.  Two row sums are kept: `l` of the fp32
-        // probabilities (for the LSE) and `l_mma` of the bf16-rounded ones that
-        // the P V product uses (for the normalisation of O, so that the rounding
-        // of a dominant probability cancels); four partial sums each.
+        // p = 2^(s c - m) two at a time, with their fp32 sum (four partial sums).
         const float2 c2 = make_float2(cj, cj);
         const float2 mneg2 = make_float2(-m, -m);
         float2 acc[4], acc_mma[4];
 #pragma unroll
         for (int a = 0; a < 4; ++a) acc[a] = acc_mma[a] = make_float2(0.f, 0.f);
+        if (C::kBlockMaxCorr) {
+          // The P V product uses bf16-rounded probabilities.  O is normalised
+          // by l plus the rounding error of each block's largest probability:
+          // a dominant probability (up to 2^8 with the stale reference) then
+          // cancels exactly between numerator and normaliser, as it would with
+          // the sum of all the rounded values, and the block's smaller
+          // probabilities leave only their small, random rounding errors.  The
+          // block maximum's exponent argument is the same fused multiply-add
+          // the loop below forms for it, so the value is bit-identical.
+          const float pbm = ex2_approx(fmaf(mx, cj, -m));
+          const float pbm_r = __uint_as_float(pack_bf16x2(pbm, 0.f) << 16);
+          lcorr = lcorr * alpha + (pbm_r - pbm);
+        }
         // (in FP8 the sums of the rounded values come from the tensor core)
         // bf16: two probabilities per 32-bit word; FP8: four (pk[c][0..7] used)
         uint32_t pk[4][16];
@@ -577,15 +596,17 @@ __global__ void __launch_bounds__(352, 1)
               pk[c][i] = pack_bf16x2(p0, p1);
             }
             acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
-            if (!C::kSumByMma)
+            if (!C::kSumByMma && !C::kBlockMaxCorr)
               acc_mma[i & 3] = __fadd2_rn(acc_mma[i & 3], make_float2(__uint_as_float(pk[c][i] << 16),
                                                                      __uint_as_float(pk[c][i] & 0xffff0000u)));
           }
         }
         const float2 accs = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        const float2 accm = __fadd2_rn(__fadd2_rn(acc_mma[0], acc_mma[1]), __fadd2_rn(acc_mma[2], acc_mma[3]));
         l = l * alpha + (accs.x + accs.y);
-        if (!C::kSumByMma) l_mma = l_mma * alpha + (accm.x + accm.y);
+        if (!C::kSumByMma && !C::kBlockMaxCorr) {
+          const float2 accm = __fadd2_rn(__fadd2_rn(acc_mma[0], acc_mma[1]), __fadd2_rn(acc_mma[2], acc_mma[3]));
+          l_mma = l_mma * alpha + (accm.x + accm.y);
+        }
         // P_t and O_t are in use until O_t += P_t(j-1) V_{j-1} has completed
         // (at j = 0 the previous item's epilogue has already waited for its
         // last product)
@@ -648,6 +669,7 @@ __global__ void __launch_bounds__(352, 1)
         reg_fence16(sv);
         l_mma = __uint_as_float(sv[0]);
       }
+      if (C::kBlockMaxCorr) l_mma = l + lcorr;
       const float inv_l = 1.f / l_mma;
       fwd_item<CAUSAL>(p, k, w);  // (recomputed rather than kept live through the loop)
       __nv_bfloat16* orow = p.o + ((size_t)w.bh * N + row_g) * D;
