@@ -19,6 +19,7 @@
 #include "fa_fwd.cuh"
 #include "fa_bwd.cuh"
 #include "fa_bwd_dq.cuh"
+#include "fa_bwd_pair.cuh"
 #include "fa_fp8.cuh"
 
 namespace {
@@ -26,6 +27,7 @@ namespace {
 std::atomic<unsigned long long> g_wait_limit_ns{0};
 std::atomic<int> g_debug_stall{0};
 std::atomic<int> g_exp2_soft_quarters{0};
+std::atomic<int> g_bwd_pair_mma{0};
 
 // caller-owned events recorded around the main kernels (profiling hook)
 struct TimingEvents {
@@ -59,14 +61,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [B*H][N][d] bf16 viewed as a 3-D tensor (d, N, B*H); boxes of 64 x 128 rows,
-// 128-byte swizzle.  Rows past N inside a head read as zero.
-bool encode_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+// [B*H][N][d] bf16 viewed as a 3-D tensor (d, N, B*H); boxes of 64 x box_rows
+// rows (128 by default), 128-byte swizzle.  Rows past N inside a head read as zero.
+bool encode_bhnd(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t elem[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, elem,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -218,6 +220,55 @@ fa_status launch_bwd(const CUtensorMap* maps, const fa::BwdParams& p, int BH, cu
   return FA_OK;
 }
 
+// dK/dV of the deterministic backward on CTA pairs (fa_bwd_pair.cuh, d = 128):
+// clusters of two CTAs on adjacent key blocks, persistent without the mask
+// (as many pairs as fit at once), one pair per item with it.
+template <bool CAUSAL>
+fa_status launch_bwd_pair(const CUtensorMap* maps, const fa::BwdParams& p, int BH, cudaStream_t stream) {
+  using C = fa::BwdPairCfg;
+  auto kernel = fa::fa_bwd_pair_kernel<CAUSAL>;
+  if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess || attr.numRegs != C::kLaunchRegs) return FA_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 2)
+    return FA_ERR_CUDA;
+  fa::BwdParams q = p;
+  const int nj = (p.nkb + 1) / 2;  // pairs of key blocks per head
+  q.num_items = nj * BH;
+  q.num_bh = BH;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute cluster_attr[1];
+  cluster_attr[0].id = cudaLaunchAttributeClusterDimension;
+  cluster_attr[0].val.clusterDim.x = 2;
+  cluster_attr[0].val.clusterDim.y = 1;
+  cluster_attr[0].val.clusterDim.z = 1;
+  cfg.attrs = cluster_attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.gridDim = dim3(2 * (unsigned)(sms / 2), 1, 1);
+  int pairs = 0;
+  if (cudaOccupancyMaxActiveClusters(&pairs, kernel, &cfg) != cudaSuccess || pairs < 1) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  q.group_heads = causal_group_heads(BH, nj, pairs);
+  const long long units = (!CAUSAL && q.num_items > pairs) ? pairs : q.num_items;
+  cfg.gridDim = dim3((unsigned)(2 * units), 1, 1);
+  const TimingEvents ev = timing_events();
+  if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_start, stream) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], q) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_stop, stream) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 template <int D, bool CAUSAL>
 fa_status launch_bwd_dq(const CUtensorMap* maps, const fa::BwdDqParams& p, int BH, cudaStream_t stream) {
   using C = fa::BwdDqCfg<D>;
@@ -305,10 +356,12 @@ fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, co
   float* dq_acc = deterministic ? nullptr : static_cast<float*>(scratch);
   float* delta_pad = reinterpret_cast<float*>(static_cast<char*>(scratch) + w.dq_bytes);
   float* lse2_pad = reinterpret_cast<float*>(static_cast<char*>(scratch) + w.dq_bytes + w.stat_bytes);
-  CUtensorMap maps[6];
+  // maps[6], maps[7]: Q and dO in boxes of 64 rows (the CTA-pair kernel's row halves)
+  CUtensorMap maps[8];
   if (!encode_bhnd(&maps[0], q, BH, N, d) || !encode_bhnd(&maps[1], k, BH, N, d) ||
       !encode_bhnd(&maps[2], v, BH, N, d) || !encode_bhnd(&maps[3], dout, BH, N, d) ||
-      !encode_f32_rows(&maps[4], lse2_pad, BH, npad, 128) || !encode_f32_rows(&maps[5], delta_pad, BH, npad, 128))
+      !encode_f32_rows(&maps[4], lse2_pad, BH, npad, 128) || !encode_f32_rows(&maps[5], delta_pad, BH, npad, 128) ||
+      !encode_bhnd(&maps[6], q, BH, N, d, 64) || !encode_bhnd(&maps[7], dout, BH, N, d, 64))
     return FA_ERR_CUDA;
   // 1. delta, LSE*log2(e) (padded), dQ accumulator = 0 (atomic dQ only)
   {
@@ -340,7 +393,9 @@ fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, co
   p.out_align32 = aligned32(dk) && aligned32(dv);
   fa_status st;
   if (deterministic) {
-    if (d == 128)
+    if (d == 128 && g_bwd_pair_mma.load())
+      st = causal ? launch_bwd_pair<true>(maps, p, BH, stream) : launch_bwd_pair<false>(maps, p, BH, stream);
+    else if (d == 128)
       st = causal ? launch_bwd<128, true, false>(maps, p, BH, stream) : launch_bwd<128, false, false>(maps, p, BH, stream);
     else
       st = causal ? launch_bwd<64, true, false>(maps, p, BH, stream) : launch_bwd<64, false, false>(maps, p, BH, stream);
@@ -406,6 +461,8 @@ const char* fa_status_string(fa_status status) {
 void fa_set_wait_limit_ns(unsigned long long limit_ns) { g_wait_limit_ns.store(limit_ns); }
 
 void fa_debug_stall(int enable) { g_debug_stall.store(enable ? 1 : 0); }
+
+void fa_set_bwd_pair_mma(int enable) { g_bwd_pair_mma.store(enable ? 1 : 0); }
 
 fa_status fa_set_exp2_split(int soft_quarters) {
   if (soft_quarters < 0 || soft_quarters > 2) return FA_ERR_INVALID_ARG;

@@ -76,6 +76,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_set_wait_limit_ns.restype = None
     lib.fa_debug_stall.argtypes = [i]
     lib.fa_debug_stall.restype = None
+    lib.fa_set_bwd_pair_mma.argtypes = [i]
+    lib.fa_set_bwd_pair_mma.restype = None
     lib.fa_set_exp2_split.argtypes = [i]
     lib.fa_set_exp2_split.restype = i
     lib.fa_set_timing_events.argtypes = [vp, vp, vp, vp]
@@ -140,6 +142,11 @@ def fa_set_wait_limit_ns(limit_ns: int) -> None:
 def fa_debug_stall(enable: bool) -> None:
     """Test hook: kernels launched while enabled stall on a barrier nothing signals."""
     load_library().fa_debug_stall(int(bool(enable)))
+
+
+def fa_set_bwd_pair_mma(enable: bool) -> None:
+    """fa_bwd_deterministic at d = 128: dK, dV products as 2-CTA (256-row) MMAs on CTA pairs."""
+    load_library().fa_set_bwd_pair_mma(int(bool(enable)))
 
 
 def fa_set_exp2_split(soft_quarters: int) -> None:

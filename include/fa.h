@@ -269,6 +269,20 @@ void fa_debug_stall(int enable);
 fa_status fa_set_exp2_split(int soft_quarters);
 
 /*
+ * How fa_bwd_deterministic forms dK and dV at d = 128 ("Interrogating the GPU
+ * part 5: FlashAttention", section "Why did Blackwell need FlashAttention-4?":
+ * the 2-SM MMA, in which two SMs compute one product of twice the rows, each
+ * reading half of the other operand from its own shared memory).  enable = 0
+ * (the default): one CTA per 128-key block, as fa_bwd.  enable != 0: clusters of
+ * two CTAs on adjacent key blocks, whose four products per query block
+ * (S^T, dP^T, dV, dK) run as 256-row tcgen05 MMAs across the pair; the
+ * results are the same up to summation order and equally bitwise repeatable.
+ * d = 64 and fa_bwd are not affected.  Process-wide; applies to calls made
+ * after it.
+ */
+void fa_set_bwd_pair_mma(int enable);
+
+/*
  * Profiling hook.  While set, fa_fwd and fa_fwd_fp8 record fwd_start and
  * fwd_stop on their stream immediately before and after launching the
  * attention kernel (not around fa_fwd_fp8's operand preparation), and fa_bwd

@@ -12,6 +12,7 @@ re-initialise them.  This file is named so that pytest collects it last.
 """
 
 import ctypes
+import gc
 import math
 
 import pytest
@@ -53,14 +54,23 @@ def test_static_scratch_matches_workspace_backward_twice(d, causal):
         assert fa.fa_check_device_status() == fa.FA_OK
         got = [torch.full_like(q, float("nan")) for _ in range(3)]
         torch.cuda.synchronize()
-        allocated = torch.cuda.memory_allocated()
-        st = lib.fa_bwd_static_scratch(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                                       lse.data_ptr(), got[0].data_ptr(), got[1].data_ptr(), got[2].data_ptr(),
-                                       B, H, N, d, ctypes.c_float(scale), int(causal),
-                                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
-        assert st == fa.FA_OK, fa.fa_status_string(st)
-        assert fa.fa_check_device_status() == fa.FA_OK
-        assert torch.cuda.memory_allocated() == allocated
+        # torch's count of allocated bytes must not move across the call.  Cyclic
+        # garbage left by earlier tests (tracebacks that hold tensors) is
+        # collected first, and the collector stays off while the count is
+        # compared, so that it cannot free tensors in between.
+        gc.collect()
+        gc.disable()
+        try:
+            allocated = torch.cuda.memory_allocated()
+            st = lib.fa_bwd_static_scratch(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                                           lse.data_ptr(), got[0].data_ptr(), got[1].data_ptr(), got[2].data_ptr(),
+                                           B, H, N, d, ctypes.c_float(scale), int(causal),
+                                           ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+            assert st == fa.FA_OK, fa.fa_status_string(st)
+            assert fa.fa_check_device_status() == fa.FA_OK
+            assert torch.cuda.memory_allocated() == allocated
+        finally:
+            gc.enable()
         for name, g, r in zip(("dq", "dk", "dv"), got, ref):
             r = r.float()
             err = (g.float() - r).abs().max().item()
