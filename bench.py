@@ -67,8 +67,10 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--e2e-chunks", type=int, default=2,
-                    help="head chunks pipelined over copy-in / compute / copy-out streams in the end-to-end leg")
+    ap.add_argument("--e2e-chunks", type=int, default=1,
+                    help="head chunks per step in the end-to-end leg (steps are pipelined over copy-in / compute / "
+                         "copy-out streams either way; more chunks also overlap copies within a step, but each "
+                         "launch then covers fewer heads)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--deterministic", action="store_true",
