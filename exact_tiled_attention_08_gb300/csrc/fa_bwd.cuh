@@ -182,17 +182,31 @@ struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kAtoms = D / 64;
   static constexpr int kSlots = (D == 128) ? (kAtomicDq ? 3 : 4) : 6;   // Q / dO ring
-  static constexpr int kStatBytes = 1024;             // LSE*log2e and delta of one query block
-  // one entry per query block whose statistics can be in use or in flight.
-  // Q_i (and its statistics) is loaded once the slot of fill 2i - kSlots is
-  // released.  With an even kSlots that fill is Q_{i - kSlots/2}, released
-  // after dK, i.e. after the elementwise step of that block: kSlots/2 entries.
+  // Statistics of a query block: 128 values of LSE*log2e (read by the first
+  // half of the elementwise step) and 128 of delta (read by the second), each
+  // in a small ring of 512-byte entries, one per query block whose values can
+  // be in use or in flight.  The L values come with Q_i (fill 2i), which is
+  // loaded once the slot of fill 2i - kSlots is released.  With an even kSlots
+  // that fill is Q_{i - kSlots/2}, released after dK, i.e. after both halves
+  // of that block's step: delta comes with Q_i too, kSlots/2 entries each.
   // With an odd kSlots it is dO_{i - (kSlots+1)/2}, released after dV, which
-  // may come before the second half of that block's elementwise step (which
-  // reads delta) has finished: one entry more.
-  static constexpr int kStatEntries = (kSlots % 2) ? (kSlots + 1) / 2 + 1 : kSlots / 2;
+  // follows the first half of that block's step: (kSlots+1)/2 L entries; delta
+  // then comes with dO_i (fill 2i + 1), loaded once Q_{i - (kSlots-1)/2} has
+  // been released by dK, after the second half: (kSlots-1)/2 delta entries.
+  static constexpr bool kDeltaWithDo = (kSlots % 2) != 0;
+  static constexpr int kLEntries = (kSlots % 2) ? (kSlots + 1) / 2 : kSlots / 2;
+  static constexpr int kDEntries = (kSlots % 2) ? (kSlots - 1) / 2 : kSlots / 2;
+  static constexpr int kStatRowBytes = 512;
+  static constexpr int kStatBytes = (kLEntries + kDEntries) * kStatRowBytes;
   static constexpr int kDsBytes = 128 * 128 * 2;      // dS^T tile: 2 atom columns of 64 queries
-  static constexpr int kStageBytes = kAtomicDq ? 4 * 4096 : 0;  // reducers' transposing tiles
+  // reducers: two 32 x 32 fp32 tiles per warp, each added to the accumulator
+  // by one TMA reduce while the warp fills the other
+  static constexpr int kStageBytes = kAtomicDq ? 4 * 2 * 4096 : 0;
+  // After the elementwise step: dQ before dK when the ring is deep enough to
+  // hold the next dO tile already (the next dP^T waits for the reducers to
+  // take dQ out of its columns).  With three slots dK goes first, because the
+  // next dO tile can only be loaded once dK has released Q_i's slot.
+  static constexpr bool kDqFirst = kSlots > 3;
   static constexpr int kThreads = 512;
   static constexpr int kLaunchRegs = 128;             // 65536 / 512
   static constexpr uint32_t kTmemCols = 512;
@@ -200,7 +214,7 @@ struct BwdCfg {
   // the dynamic shared memory is declared 1024-byte aligned (checked at run
   // time), so no alignment slack is added
   static constexpr int kSmemBytes =
-      2 * kTileBytes + kSlots * kTileBytes + kDsBytes + kStageBytes + kStatEntries * kStatBytes + 256;
+      2 * kTileBytes + kSlots * kTileBytes + kDsBytes + kStageBytes + kStatBytes + 256;
 };
 
 struct BwdBarriers {
@@ -271,7 +285,7 @@ __global__ void __launch_bounds__(512, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                   const __grid_constant__ CUtensorMap map_lse2, const __grid_constant__ CUtensorMap map_delta,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap map_dq, const BwdParams p) {
   using C = BwdCfg<D, kAtomicDq>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {
@@ -285,9 +299,10 @@ __global__ void __launch_bounds__(512, 1)
   uint8_t* sRing = smem + 2 * C::kTileBytes;
   uint8_t* sDS = sRing + C::kSlots * C::kTileBytes;
   uint8_t* sStage = sDS + C::kDsBytes;
-  // query block it: entry it % kStatEntries = LSE*log2e [128], delta [128]
-  uint8_t* sStat = sStage + C::kStageBytes;
-  BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(sStat + C::kStatEntries * C::kStatBytes);
+  // query block g: LSE*log2e in L entry g % kLEntries, delta in entry g % kDEntries
+  uint8_t* sStatL = sStage + C::kStageBytes;
+  uint8_t* sStatD = sStatL + C::kLEntries * C::kStatRowBytes;
+  BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(sStatL + C::kStatBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N;
@@ -324,6 +339,7 @@ __global__ void __launch_bounds__(512, 1)
     tma_prefetch_map(&map_do);
     tma_prefetch_map(&map_lse2);
     tma_prefetch_map(&map_delta);
+    if (kAtomicDq) tma_prefetch_map(&map_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -365,7 +381,9 @@ __global__ void __launch_bounds__(512, 1)
                 ok = false;
                 break;
               }
-              mbar_arrive_expect_tx(&bar->ring_full[s], C::kTileBytes + (which ? 0 : C::kStatBytes));
+              const bool with_l = !which, with_d = (which != 0) == C::kDeltaWithDo;
+              mbar_arrive_expect_tx(&bar->ring_full[s],
+                                    C::kTileBytes + (with_l ? C::kStatRowBytes : 0) + (with_d ? C::kStatRowBytes : 0));
               const CUtensorMap* map = which ? &map_do : &map_q;
               for (int a = 0; a < C::kAtoms; ++a)
                 tma_load_3d(sRing + s * C::kTileBytes + a * 16384, map, &bar->ring_full[s], a * 64, i * 128, t.bh);
@@ -374,13 +392,15 @@ __global__ void __launch_bounds__(512, 1)
               // served from L2
               if (C::kSlots < 4 && it + 1 < t.n_it)
                 for (int a = 0; a < C::kAtoms; ++a) tma_prefetch_l2_3d(map, a * 64, (i + 1) * 128, t.bh);
-              if (!which) {
-                // the entry was last read by the elementwise step of block
-                // g - kStatEntries, which has finished once this slot is free
-                uint8_t* st = sStat + (g % C::kStatEntries) * C::kStatBytes;
-                tma_load_2d(st, &map_lse2, &bar->ring_full[s], i * 128, t.bh);
-                tma_load_2d(st + 512, &map_delta, &bar->ring_full[s], i * 128, t.bh);
-              }
+              // the entries were last read by the elementwise step of block
+              // g - kLEntries (g - kDEntries), which has read them once this
+              // slot is free (see BwdCfg)
+              if (with_l)
+                tma_load_2d(sStatL + (g % C::kLEntries) * C::kStatRowBytes, &map_lse2, &bar->ring_full[s], i * 128,
+                            t.bh);
+              if (with_d)
+                tma_load_2d(sStatD + (g % C::kDEntries) * C::kStatRowBytes, &map_delta, &bar->ring_full[s], i * 128,
+                            t.bh);
               ++fill;
             }
           }
@@ -426,6 +446,7 @@ __global__ void __launch_bounds__(512, 1)
                   ok = false;
                   break;
                 }
+
                 tc_fence_after();
                 const uint64_t qdesc = sdesc_sw128(ring + sq * C::kTileBytes, 16, 1024);
 #pragma unroll
@@ -434,6 +455,7 @@ __global__ void __launch_bounds__(512, 1)
                   mma_bf16_ss(tS, kdesc + off, qdesc + off, id_s, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar->s_full);
+
               } else {
                 // dP^T = V dO_i^T, once the reducers have taken the previous dQ
                 // out of these columns (without dQ: once the elementwise step
@@ -498,18 +520,13 @@ __global__ void __launch_bounds__(512, 1)
             mma_commit(&bar->dv_done);
             mma_commit(&bar->ring_empty[sd]);
             // dQ_i = dS K (into the dP^T columns, read by now) and dK += dS^T Q_i,
-            // once dS^T is written.  dQ goes first when the ring is deep enough
-            // to have the next dO tile already: the next dP^T waits for the
-            // reducers to take dQ out of these columns.  With a three-slot ring
-            // dK goes first, because the next dO tile can only be loaded once
-            // dK has released Q_i's slot.
+            // once dS^T is written, in the order BwdCfg gives
             if (!(ok = wait_bounded_inl(&bar->ew_done, g & 1, ctx, kSiteBwdEw))) break;
             tc_fence_after();
             const uint64_t qdesc_mn = sdesc_sw128(ring + sq * C::kTileBytes, 16384, 1024);
-            constexpr bool kDqFirst = C::kSlots > 3;
 #pragma unroll
             for (int step = 0; step < 2; ++step) {
-              if ((step == 0) == kDqFirst) {
+              if ((step == 0) == C::kDqFirst) {
                 if (kAtomicDq) {
 #pragma unroll
                   for (int kk = 0; kk < 8; ++kk)
@@ -548,11 +565,10 @@ __global__ void __launch_bounds__(512, 1)
     setmaxnreg_inc<kBwdRedRegs>();
     const int q = warp & 3;
     const uint32_t tDQ = tmem + C::kDpCol + ((uint32_t)(q * 32) << 16);
-    uint8_t* stage = sStage + q * 4096;
-    const int chunk = lane & 7;
-    constexpr int kChunks = D / 32;  // 32-column chunks of a dQ row
+    uint8_t* stage = sStage + q * 8192;  // two 4 KB tiles
+    constexpr int kChunks = D / 32;      // 32-column chunks of a dQ row
     bool alive = true;
-    int g = 0;
+    int g = 0, r = 0;                    // r: tiles handed to the TMA so far
     for (int item = blockIdx.x; alive && item < p.num_items; item += gridDim.x) {
       const BwdItem t = bwd_item<CAUSAL>(p, item);
       for (int it = 0; it < t.n_it; ++it, ++g) {
@@ -570,28 +586,38 @@ __global__ void __launch_bounds__(512, 1)
         // dQ_i is in registers: issuer A may overwrite these columns with dP^T
         tc_fence_before();
         mbar_arrive(&bar->dq_free);
-        // thread = query row 32 q + lane; each 32 x 32 block goes through the
-        // stage (row-major, 16-byte chunks swizzled by row) and comes back with
-        // 8 lanes per row, so that each reduction covers four whole 128-byte lines
+        // thread = query row 32 q + lane.  Each 32 x 32 block goes to a stage
+        // tile in the TMA's 128-byte-swizzled layout (row = lane, 16-byte chunk
+        // j at position j ^ (row & 7)), and one TMA reduce adds the tile to the
+        // accumulator (rows past N are not written).  The two tiles alternate:
+        // before a tile is refilled, the reduce issued from it two chunks ago
+        // must have read it.
         const int qrow0 = (t.i_start + it) * 128 + 32 * q;
-        float* acc_rows = p.dq_acc + ((size_t)t.bh * N + qrow0) * D;
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
+        for (int c = 0; c < kChunks; ++c, ++r) {
+          uint8_t* tile = stage + (r & 1) * 4096;
+          if (r >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
 #pragma unroll
           for (int c16 = 0; c16 < 8; ++c16)
-            *reinterpret_cast<uint4*>(stage + lane * 128 + ((c16 ^ (lane & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(tile + lane * 128 + ((c16 ^ (lane & 7)) << 4)) =
                 make_uint4(dqv[c][4 * c16], dqv[c][4 * c16 + 1], dqv[c][4 * c16 + 2], dqv[c][4 * c16 + 3]);
+          fence_async_shared();
           __syncwarp();
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int row = 4 * k + (lane >> 3);
-            const float4 x = *reinterpret_cast<const float4*>(stage + row * 128 + ((chunk ^ (row & 7)) << 4));
-            if (qrow0 + row < N) red_add_v4(acc_rows + (size_t)row * D + 32 * c + 4 * chunk, x.x, x.y, x.z, x.w);
+          if (lane == 0) {
+            // (a tile wholly past N, in the last block of a head, is not sent;
+            // its group is empty)
+            if (qrow0 < N) tma_reduce_add_3d(&map_dq, tile, 32 * c, qrow0, t.bh);
+            tma_store_commit();
           }
-          __syncwarp();
         }
       }
     }
+    // every reduce has completed (and read its tile) before the CTA ends
+    if (lane == 0) tma_store_wait_all();
+    __syncwarp();
     }
   } else {
     // ------------------------------------------------------------------ elementwise
@@ -609,7 +635,8 @@ __global__ void __launch_bounds__(512, 1)
     for (int item = blockIdx.x; alive && item < p.num_items; item += gridDim.x, ++w) {
       const BwdItem t = bwd_item<CAUSAL>(p, item);
       for (int it = 0; alive && it < t.n_it; ++it, ++g) {
-        const float* stat = reinterpret_cast<const float*>(sStat + (g % C::kStatEntries) * C::kStatBytes);
+        const float* statL = reinterpret_cast<const float*>(sStatL + (g % C::kLEntries) * C::kStatRowBytes);
+        const float* statD = reinterpret_cast<const float*>(sStatD + (g % C::kDEntries) * C::kStatRowBytes);
         // ---- phase 1: P^T = 2^(S^T c - L log2e) into TMEM, the fp32 values kept
         // in registers; issuer B starts dV as soon as all of P^T is written
         if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->s_full, g & 1, ctx, kSiteBwdS))) {
@@ -631,7 +658,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             // four queries' L*log2e (the same for every thread: a broadcast read)
-            const float4 l4 = *reinterpret_cast<const float4*>(stat + qc + 4 * e4);
+            const float4 l4 = *reinterpret_cast<const float4*>(statL + qc + 4 * e4);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int e = 4 * e4 + 2 * h;  // two queries at a time (packed fp32x2 arithmetic)
@@ -675,7 +702,7 @@ __global__ void __launch_bounds__(512, 1)
           uint32_t dk[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(stat + 128 + qc + 4 * e4);
+            const float4 d4 = *reinterpret_cast<const float4*>(statD + qc + 4 * e4);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int e = 4 * e4 + 2 * h;

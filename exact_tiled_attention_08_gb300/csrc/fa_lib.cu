@@ -214,7 +214,7 @@ fa_status launch_bwd(const CUtensorMap* maps, const fa::BwdParams& p, int BH, cu
   const TimingEvents ev = timing_events();
   if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_start, stream) != cudaSuccess) return FA_ERR_CUDA;
   kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                                                                  q);
+                                                                  maps[8], q);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   if (ev.bwd_start && ev.bwd_stop && cudaEventRecord(ev.bwd_stop, stream) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
@@ -284,6 +284,21 @@ fa_status launch_bwd_dq(const CUtensorMap* maps, const fa::BwdDqParams& p, int B
   const long long grid = (long long)p.nqb * BH;
   kernel<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(maps[0], maps[1], maps[2], maps[3], q);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// the fp32 dQ accumulator [B*H][N][d] viewed as a 3-D tensor (d, N, B*H); boxes
+// of 32 x 32 rows, 128-byte swizzle (the backward's reducers add such tiles
+// with TMA reduces; rows past N inside a head are not written)
+bool encode_dq_acc(CUtensorMap* map, const float* ptr, int BH, int N, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // fp32 [rows][cols] viewed as a 2-D tensor (cols, rows); boxes of box_cols x 1, no swizzle
@@ -356,13 +371,17 @@ fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, co
   float* dq_acc = deterministic ? nullptr : static_cast<float*>(scratch);
   float* delta_pad = reinterpret_cast<float*>(static_cast<char*>(scratch) + w.dq_bytes);
   float* lse2_pad = reinterpret_cast<float*>(static_cast<char*>(scratch) + w.dq_bytes + w.stat_bytes);
-  // maps[6], maps[7]: Q and dO in boxes of 64 rows (the CTA-pair kernel's row halves)
-  CUtensorMap maps[8];
+  // maps[6], maps[7]: Q and dO in boxes of 64 rows (the CTA-pair kernel's row halves);
+  // maps[8]: the dQ accumulator (atomic dQ only; otherwise a copy of maps[0] that
+  // nothing reads)
+  CUtensorMap maps[9];
   if (!encode_bhnd(&maps[0], q, BH, N, d) || !encode_bhnd(&maps[1], k, BH, N, d) ||
       !encode_bhnd(&maps[2], v, BH, N, d) || !encode_bhnd(&maps[3], dout, BH, N, d) ||
       !encode_f32_rows(&maps[4], lse2_pad, BH, npad, 128) || !encode_f32_rows(&maps[5], delta_pad, BH, npad, 128) ||
       !encode_bhnd(&maps[6], q, BH, N, d, 64) || !encode_bhnd(&maps[7], dout, BH, N, d, 64))
     return FA_ERR_CUDA;
+  if (dq_acc && !encode_dq_acc(&maps[8], dq_acc, BH, N, d)) return FA_ERR_CUDA;
+  if (!dq_acc) maps[8] = maps[0];
   // 1. delta, LSE*log2(e) (padded), dQ accumulator = 0 (atomic dQ only)
   {
     const long long padded_rows = (long long)BH * npad;
