@@ -207,6 +207,13 @@ struct BwdCfg {
   // take dQ out of its columns).  With three slots dK goes first, because the
   // next dO tile can only be loaded once dK has released Q_i's slot.
   static constexpr bool kDqFirst = kSlots > 3;
+  // d = 128 with the atomic dQ: the elementwise step also writes dS^T as bf16
+  // into the half of the S^T columns that P^T leaves free, and dK takes its A
+  // operand from there (half the shared-memory reads of dK); the next block's
+  // S^T then waits for dK as well as dV.  Holding the next S^T back until dK
+  // has run also keeps it from sharing the tensor pipe with dK, whose slot
+  // release starts the next dO load.
+  static constexpr bool kDsTmem = D == 128 && kAtomicDq;
   static constexpr int kThreads = 512;
   static constexpr int kLaunchRegs = 128;             // 65536 / 512
   static constexpr uint32_t kTmemCols = 512;
@@ -435,14 +442,18 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
             for (int step = 0; step < 2; ++step) {
               if (step == 0) {
-                // S^T = K Q_i^T, once dV has consumed the previous P^T held in
-                // these columns
+                // S^T = K Q_i^T, once dV (and dK, kDsTmem) have consumed the
+                // previous P^T (dS^T) held in these columns
                 const int fq = 2 * g, sq = fq % C::kSlots;
                 if (!wait_bounded_inl(&bar->ring_full[sq], (fq / C::kSlots) & 1, ctx, kSiteBwdQ)) {
                   ok = false;
                   break;
                 }
                 if (g > 0 && !wait_bounded_inl(&bar->dv_done, (g - 1) & 1, ctx, kSiteBwdDvDone)) {
+                  ok = false;
+                  break;
+                }
+                if (C::kDsTmem && g > 0 && !wait_bounded_inl(&bar->dk_done, (g - 1) & 1, ctx, kSiteBwdDvDone)) {
                   ok = false;
                   break;
                 }
@@ -538,8 +549,12 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                   const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                  mma_bf16_ss(tDK, dsdesc_k + off, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
-                              (it > 0 || kk > 0) ? 1u : 0u);
+                  if (C::kDsTmem)  // dS^T of query group kk at S^T column 16 kk + 8
+                    mma_bf16_ts(tDK, tS + kk * 16 + 8, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
+                                (it > 0 || kk > 0) ? 1u : 0u);
+                  else
+                    mma_bf16_ss(tDK, dsdesc_k + off, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
+                                (it > 0 || kk > 0) ? 1u : 0u);
                 }
                 // Q_i has been read by S^T (long complete) and dK: release its
                 // slot; the dS^T tile is free for the next elementwise step once
@@ -681,7 +696,8 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_before();
         mbar_arrive(&bar->p_done);
 
-        // ---- phase 2: dS^T = P^T o (dP^T - delta) into the shared dS^T tile,
+        // ---- phase 2: dS^T = P^T o (dP^T - delta) into the shared dS^T tile
+        // (and, kDsTmem, beside P^T in TMEM, for dK),
         // once the previous block's dK and dQ have read it (dP^T of this block
         // was issued after the reducers took the previous dQ out of TMEM; dK,
         // which runs after dQ, reports on its own)
@@ -719,8 +735,13 @@ __global__ void __launch_bounds__(512, 1)
             *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
                 make_uint4(dk[4 * c16], dk[4 * c16 + 1], dk[4 * c16 + 2], dk[4 * c16 + 3]);
           }
+          if (C::kDsTmem) {  // beside P^T: columns qc + 8 and qc + 24 onwards, 8 each
+            tmem_st8(tS + qc + 8, dk);
+            tmem_st8(tS + qc + 24, dk + 8);
+          }
         }
         fence_async_shared();
+        if (C::kDsTmem) tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar->ew_done);
       }
