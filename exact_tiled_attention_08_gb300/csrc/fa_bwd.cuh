@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(256)
 // to nkb query blocks; bwd_item hands the costliest out first and the
 // hardware's CTA scheduler balances them); without it the CTAs are
 // persistent, one per SM, and walk the items blockIdx.x, blockIdx.x +
-// gridDim.x, ...  All pipeline counters (ring fills, per-block barrier
+// gridDim.x, ...  All pipeline counters (slot uses, per-block barrier
 // phases, statistics entries) run on across the items: a CTA loads the next
 // item's K and V, then its first Q tile, as soon as the current item's last
 // dK and dQ products have read the old K and V, and the reducers' last dQ_i
@@ -125,39 +125,39 @@ __global__ void __launch_bounds__(256)
 //
 // K_j and V_j (128 keys) stay in shared memory; the query blocks i (all of
 // them, or i >= j when causal) stream Q_i (with its rows' LSE log2(e) and
-// delta) and dO_i through a ring.  Per query block, in the transposed
+// delta) and dO_i through slots of their own (BwdCfg).  Per query block, in the transposed
 // orientation (TMEM lane = key, column = query):
 //   S^T = K_j Q_i^T, then dP^T = V_j dO_i^T      (issuer A)
 //   P^T  = 2^(S^T scale log2e - LSE_i log2e), masked on the causal diagonal
 //                                                  (elementwise warps, thread = key)
 //   dV += P^T dO_i                                 (issuer B, as soon as P^T is written)
 //   dS^T = P^T o (dP^T - delta_i)                  (elementwise warps)
-//   dQ_i = dS K_j and dK += dS^T Q_i              (issuer B)
+//   dQ_i = dS K_j, then dK += dS^T Q_i            (issuer B)
 // and the reducer warps add dQ_i into the fp32 accumulator in global memory
 // while the next query block is processed.  The elementwise step is split in
 // two so that dV runs while dS^T is computed, and the next block's S^T (whose
 // columns dV frees) while dK and dQ run.  dK, dV accumulate in TMEM across
 // the item's query blocks and are written once at the end of the item.
 //
-// The global fp32 reduction of dQ_i (64 KB per query block at d = 128) is
-// bound by the L2's atomic throughput, which is close to the time the rest of
-// a query block takes; it therefore runs on warps of its own that hold dQ_i in
-// registers, so that TMEM is free for the next dP^T at once and the
-// elementwise warps never wait for it.
+// The global fp32 reduction of dQ_i (64 KB per query block at d = 128) takes
+// about as long as the rest of a query block; it therefore runs on warps of
+// its own that hold dQ_i in registers, so that TMEM is free for the next dP^T
+// at once and the elementwise warps never wait for it, and it goes through
+// TMA reduces, off the load/store path the elementwise warps' shared-memory
+// stores use.
 //
 // Warp roles (512 threads, four warpgroups; register budgets set with
 // setmaxnreg, 144 + 144 + 152 + 72 per thread = the launch's 128 x 4):
 //   warps 0-7   elementwise: warpgroup g owns query columns [64 g, 64 g + 64)
 //               of dS
 //   warps 8-11  reducers: warp 8 + q takes TMEM lanes 32q.. (query rows) of
-//               dQ_i into registers, releases the columns, transposes 32 x 32
-//               blocks through its own 4 KB of shared memory so that 8 lanes
-//               cover one 128-byte row segment, and adds them with
-//               red.global.add.v4.f32, four whole lines per instruction
+//               dQ_i into registers, releases the columns, writes 32 x 32
+//               blocks into two 4 KB tiles of its own in the TMA's swizzled
+//               layout and adds each to the accumulator with one TMA reduce
 //   warp  12    issuer A (S^T and dP^T) and TMEM owner
-//   warp  13    TMA producer
+//   warp  13    TMA producer: K, V and the Q tiles
 //   warp  14    issuer B (dV, dQ and dK)
-//   warp  15    idle
+//   warp  15    TMA producer: the dO tiles
 // Tensor memory: dK at column 0, dV at d, S^T at 2d, dP^T at 2d + 128.  The
 // bf16 P^T of query group G (queries 16G..16G+15) is written over the first 8
 // of that group's own S^T columns, which only the writing thread has read;
@@ -176,44 +176,28 @@ static_assert(2 * kBwdWorkRegs + kBwdRedRegs + kBwdMiscRegs == 4 * 128, "registe
 // kAtomicDq: the kernel also forms dQ_i = dS K_j and adds it into the fp32
 // accumulator (reducer warps); otherwise dQ is left to the separate
 // deterministic pass, and the shared memory of the reducers' staging tiles
-// goes to a fourth ring slot at d = 128.
+// goes to a fourth tile slot (a second dO slot) at d = 128.
 template <int D, bool kAtomicDq>
 struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kAtoms = D / 64;
-  static constexpr int kSlots = (D == 128) ? (kAtomicDq ? 3 : 4) : 6;   // Q / dO ring
-  // Statistics of a query block: 128 values of LSE*log2e (read by the first
-  // half of the elementwise step) and 128 of delta (read by the second), each
-  // in a small ring of 512-byte entries, one per query block whose values can
-  // be in use or in flight.  The L values come with Q_i (fill 2i), which is
-  // loaded once the slot of fill 2i - kSlots is released.  With an even kSlots
-  // that fill is Q_{i - kSlots/2}, released after dK, i.e. after both halves
-  // of that block's step: delta comes with Q_i too, kSlots/2 entries each.
-  // With an odd kSlots it is dO_{i - (kSlots+1)/2}, released after dV, which
-  // follows the first half of that block's step: (kSlots+1)/2 L entries; delta
-  // then comes with dO_i (fill 2i + 1), loaded once Q_{i - (kSlots-1)/2} has
-  // been released by dK, after the second half: (kSlots-1)/2 delta entries.
-  static constexpr bool kDeltaWithDo = (kSlots % 2) != 0;
-  static constexpr int kLEntries = (kSlots % 2) ? (kSlots + 1) / 2 : kSlots / 2;
-  static constexpr int kDEntries = (kSlots % 2) ? (kSlots - 1) / 2 : kSlots / 2;
-  static constexpr int kStatRowBytes = 512;
-  static constexpr int kStatBytes = (kLEntries + kDEntries) * kStatRowBytes;
+  static constexpr int kSlots = (D == 128) ? (kAtomicDq ? 3 : 4) : 6;   // Q and dO tiles
+  // Q tiles and dO tiles have slots of their own: Q_g goes to Q slot
+  // g % kQSlots once dK of block g - kQSlots has released it, dO_g to dO slot
+  // g % kDoSlots once dV of block g - kDoSlots has.  dV runs right after the
+  // first half of the elementwise step, so with three slots (two for Q, one
+  // for dO) the next dO tile loads while the second half and dQ, dK run, and
+  // the next Q tile is a whole block ahead.
+  static constexpr int kQSlots = (kSlots + 1) / 2, kDoSlots = kSlots / 2;
+  // LSE*log2e [128] and delta [128] of a query block come with its Q tile; the
+  // entry of block g is reused by block g + kQSlots, whose Q loads once dK of
+  // block g, which follows its elementwise step, has run
+  static constexpr int kStatBytes = 1024;
+  static constexpr int kStatEntries = kQSlots;
   static constexpr int kDsBytes = 128 * 128 * 2;      // dS^T tile: 2 atom columns of 64 queries
   // reducers: two 32 x 32 fp32 tiles per warp, each added to the accumulator
   // by one TMA reduce while the warp fills the other
   static constexpr int kStageBytes = kAtomicDq ? 4 * 2 * 4096 : 0;
-  // After the elementwise step: dQ before dK when the ring is deep enough to
-  // hold the next dO tile already (the next dP^T waits for the reducers to
-  // take dQ out of its columns).  With three slots dK goes first, because the
-  // next dO tile can only be loaded once dK has released Q_i's slot.
-  static constexpr bool kDqFirst = kSlots > 3;
-  // d = 128 with the atomic dQ: the elementwise step also writes dS^T as bf16
-  // into the half of the S^T columns that P^T leaves free, and dK takes its A
-  // operand from there (half the shared-memory reads of dK); the next block's
-  // S^T then waits for dK as well as dV.  Holding the next S^T back until dK
-  // has run also keeps it from sharing the tensor pipe with dK, whose slot
-  // release starts the next dO load.
-  static constexpr bool kDsTmem = D == 128 && kAtomicDq;
   static constexpr int kThreads = 512;
   static constexpr int kLaunchRegs = 128;             // 65536 / 512
   static constexpr uint32_t kTmemCols = 512;
@@ -221,7 +205,7 @@ struct BwdCfg {
   // the dynamic shared memory is declared 1024-byte aligned (checked at run
   // time), so no alignment slack is added
   static constexpr int kSmemBytes =
-      2 * kTileBytes + kSlots * kTileBytes + kDsBytes + kStageBytes + kStatBytes + 256;
+      2 * kTileBytes + kSlots * kTileBytes + kDsBytes + kStageBytes + kStatEntries * kStatBytes + 256;
 };
 
 struct BwdBarriers {
@@ -306,10 +290,9 @@ __global__ void __launch_bounds__(512, 1)
   uint8_t* sRing = smem + 2 * C::kTileBytes;
   uint8_t* sDS = sRing + C::kSlots * C::kTileBytes;
   uint8_t* sStage = sDS + C::kDsBytes;
-  // query block g: LSE*log2e in L entry g % kLEntries, delta in entry g % kDEntries
-  uint8_t* sStatL = sStage + C::kStageBytes;
-  uint8_t* sStatD = sStatL + C::kLEntries * C::kStatRowBytes;
-  BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(sStatL + C::kStatBytes);
+  // query block g: entry g % kStatEntries = LSE*log2e [128], delta [128]
+  uint8_t* sStat = sStage + C::kStageBytes;
+  BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(sStat + C::kStatEntries * C::kStatBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.N;
@@ -355,68 +338,53 @@ __global__ void __launch_bounds__(512, 1)
   const WaitCtx ctx{&bar->abort_flag, p.wait_limit_ns};
   if (warp >= 12) {
     setmaxnreg_dec<kBwdMiscRegs>();
-    if (warp == 13) {
-      // ---------------------------------------------------------------- TMA producer
-      // ring fills, counted over all of the CTA's items: the g-th query
-      // block's Q_i (with its LSE*log2e and delta rows) at 2 g, dO_i at
-      // 2 g + 1.
+    if (warp == 13 || warp == 15) {
+      // ---------------------------------------------------------------- TMA producers
+      // warp 13: K and V of each item and the Q tiles (with the statistics),
+      // warp 15: the dO tiles, so that neither queue waits on the other's
+      // slot.  g counts query blocks over all of the CTA's items.
       if (lane == 0) {
-        int fill = 0, g = 0, w = 0, kv_loads = 0;
+        const bool q_side = warp == 13;
+        const int nslot = q_side ? C::kQSlots : C::kDoSlots, slot0 = q_side ? 0 : C::kQSlots;
+        int g = 0, w = 0, kv_loads = 0;
         bool ok = true;
         for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x, ++w) {
           const BwdItem t = bwd_item<CAUSAL>(p, item);
-          for (int it = 0; ok && it < t.n_it; ++it, ++g) {
+          if (q_side) {
+            // K and V of the item, once the previous item's last products
+            // (acc_done) have read the old ones
+            if (w > 0 && !wait_bounded_inl(&bar->acc_done, (w - 1) & 1, ctx, kSiteBwdProducer)) break;
+            mbar_arrive_expect_tx(&bar->kv_full, 2 * C::kTileBytes);
+            for (int a = 0; a < C::kAtoms; ++a) {
+              tma_load_3d(sK + a * 16384, &map_k, &bar->kv_full, a * 64, t.jb * 128, t.bh);
+              tma_load_3d(sV + a * 16384, &map_v, &bar->kv_full, a * 64, t.jb * 128, t.bh);
+            }
+            ++kv_loads;
+          }
+          for (int it = 0; it < t.n_it; ++it, ++g) {
             const int i = t.i_start + it;
-            for (int which = 0; which < 2; ++which) {
-              // K and V of the item go first, once the previous item's last
-              // products (acc_done) have read the old ones
-              if (!which && it == 0) {
-                if (w > 0 && !wait_bounded_inl(&bar->acc_done, (w - 1) & 1, ctx, kSiteBwdProducer)) {
-                  ok = false;
-                  break;
-                }
-                mbar_arrive_expect_tx(&bar->kv_full, 2 * C::kTileBytes);
-                for (int a = 0; a < C::kAtoms; ++a) {
-                  tma_load_3d(sK + a * 16384, &map_k, &bar->kv_full, a * 64, t.jb * 128, t.bh);
-                  tma_load_3d(sV + a * 16384, &map_v, &bar->kv_full, a * 64, t.jb * 128, t.bh);
-                }
-                ++kv_loads;
-              }
-              const int s = fill % C::kSlots;
-              const uint32_t u = fill / C::kSlots;
-              if (!wait_bounded_inl(&bar->ring_empty[s], (u & 1) ^ 1, ctx, kSiteBwdProducer)) {
-                ok = false;
-                break;
-              }
-              const bool with_l = !which, with_d = (which != 0) == C::kDeltaWithDo;
-              mbar_arrive_expect_tx(&bar->ring_full[s],
-                                    C::kTileBytes + (with_l ? C::kStatRowBytes : 0) + (with_d ? C::kStatRowBytes : 0));
-              const CUtensorMap* map = which ? &map_do : &map_q;
-              for (int a = 0; a < C::kAtoms; ++a)
-                tma_load_3d(sRing + s * C::kTileBytes + a * 16384, map, &bar->ring_full[s], a * 64, i * 128, t.bh);
-              // with a three-slot ring the same tile of the next query block goes
-              // to L2 now, so that its load (which waits for a free slot) is
-              // served from L2
-              if (C::kSlots < 4 && it + 1 < t.n_it)
-                for (int a = 0; a < C::kAtoms; ++a) tma_prefetch_l2_3d(map, a * 64, (i + 1) * 128, t.bh);
-              // the entries were last read by the elementwise step of block
-              // g - kLEntries (g - kDEntries), which has read them once this
-              // slot is free (see BwdCfg)
-              if (with_l)
-                tma_load_2d(sStatL + (g % C::kLEntries) * C::kStatRowBytes, &map_lse2, &bar->ring_full[s], i * 128,
-                            t.bh);
-              if (with_d)
-                tma_load_2d(sStatD + (g % C::kDEntries) * C::kStatRowBytes, &map_delta, &bar->ring_full[s], i * 128,
-                            t.bh);
-              ++fill;
+            const int s = slot0 + g % nslot;
+            if (!wait_bounded_inl(&bar->ring_empty[s], ((g / nslot) & 1) ^ 1, ctx, kSiteBwdProducer)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bar->ring_full[s], C::kTileBytes + (q_side ? C::kStatBytes : 0));
+            const CUtensorMap* map = q_side ? &map_q : &map_do;
+            for (int a = 0; a < C::kAtoms; ++a)
+              tma_load_3d(sRing + s * C::kTileBytes + a * 16384, map, &bar->ring_full[s], a * 64, i * 128, t.bh);
+            if (q_side) {
+              uint8_t* st = sStat + (g % C::kStatEntries) * C::kStatBytes;
+              tma_load_2d(st, &map_lse2, &bar->ring_full[s], i * 128, t.bh);
+              tma_load_2d(st + 512, &map_delta, &bar->ring_full[s], i * 128, t.bh);
             }
           }
         }
+        // every load this warp started has landed before the CTA may end
         if (kv_loads > 0) wait_drain_inl(&bar->kv_full, (kv_loads - 1) & 1, kDrainLimitNs);
-        for (int s = 0; s < C::kSlots; ++s) {
-          if (fill > s) {
-            const int uses = (fill - 1 - s) / C::kSlots + 1;
-            wait_drain_inl(&bar->ring_full[s], (uses - 1) & 1, kDrainLimitNs);
+        for (int k = 0; k < nslot; ++k) {
+          if (g > k) {
+            const int uses = (g - 1 - k) / nslot + 1;
+            wait_drain_inl(&bar->ring_full[slot0 + k], (uses - 1) & 1, kDrainLimitNs);
           }
         }
       }
@@ -432,7 +400,8 @@ __global__ void __launch_bounds__(512, 1)
         bool ok = !(p.debug_stall && !wait_bounded_inl(&bar->never, 0, ctx, kSiteStall));
         // S^T goes first: the first half of the elementwise step needs only
         // S^T, its columns are free as soon as dV of the previous block has
-        // run, and (with a three-slot ring) dO_i may still be on its way.
+        // run, and dP^T waits for the reducers to take the previous dQ out of
+        // its columns.
         // g counts query blocks over all of the CTA's items, w the items.
         int g = 0, w = 0;
         for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x, ++w) {
@@ -442,10 +411,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
             for (int step = 0; step < 2; ++step) {
               if (step == 0) {
-                // S^T = K Q_i^T, once dV (and dK, kDsTmem) have consumed the
-                // previous P^T (dS^T) held in these columns
-                const int fq = 2 * g, sq = fq % C::kSlots;
-                if (!wait_bounded_inl(&bar->ring_full[sq], (fq / C::kSlots) & 1, ctx, kSiteBwdQ)) {
+                // S^T = K Q_i^T, once dV has consumed the previous P^T held in
+                // these columns
+                const int sq = g % C::kQSlots;
+                if (!wait_bounded_inl(&bar->ring_full[sq], (g / C::kQSlots) & 1, ctx, kSiteBwdQ)) {
                   ok = false;
                   break;
                 }
@@ -453,11 +422,6 @@ __global__ void __launch_bounds__(512, 1)
                   ok = false;
                   break;
                 }
-                if (C::kDsTmem && g > 0 && !wait_bounded_inl(&bar->dk_done, (g - 1) & 1, ctx, kSiteBwdDvDone)) {
-                  ok = false;
-                  break;
-                }
-
                 tc_fence_after();
                 const uint64_t qdesc = sdesc_sw128(ring + sq * C::kTileBytes, 16, 1024);
 #pragma unroll
@@ -466,13 +430,12 @@ __global__ void __launch_bounds__(512, 1)
                   mma_bf16_ss(tS, kdesc + off, qdesc + off, id_s, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar->s_full);
-
               } else {
                 // dP^T = V dO_i^T, once the reducers have taken the previous dQ
                 // out of these columns (without dQ: once the elementwise step
                 // has read the previous dP^T)
-                const int fd = 2 * g + 1, sd = fd % C::kSlots;
-                if (!wait_bounded_inl(&bar->ring_full[sd], (fd / C::kSlots) & 1, ctx, kSiteBwdDo)) {
+                const int sd = C::kQSlots + g % C::kDoSlots;
+                if (!wait_bounded_inl(&bar->ring_full[sd], (g / C::kDoSlots) & 1, ctx, kSiteBwdDo)) {
                   ok = false;
                   break;
                 }
@@ -513,7 +476,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
           const BwdItem t = bwd_item<CAUSAL>(p, item);
           for (int it = 0; ok && it < t.n_it; ++it, ++g) {
-            const int sq = (2 * g) % C::kSlots, sd = (2 * g + 1) % C::kSlots;
+            const int sq = g % C::kQSlots, sd = C::kQSlots + g % C::kDoSlots;
             // dV += P^T dO_i as soon as the elementwise warps have written P^T
             // (P^T of query group kk sits at S^T column 16 kk) and dP^T, which
             // also reads dO_i, is complete (so dO_i has landed, and its slot can
@@ -530,39 +493,33 @@ __global__ void __launch_bounds__(512, 1)
                           (it > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&bar->dv_done);
             mma_commit(&bar->ring_empty[sd]);
-            // dQ_i = dS K (into the dP^T columns, read by now) and dK += dS^T Q_i,
-            // once dS^T is written, in the order BwdCfg gives
+            // dQ_i = dS K (into the dP^T columns, read by now; the next dP^T
+            // waits for the reducers to take it out), then dK += dS^T Q_i, once
+            // dS^T is written
             if (!(ok = wait_bounded_inl(&bar->ew_done, g & 1, ctx, kSiteBwdEw))) break;
             tc_fence_after();
-            const uint64_t qdesc_mn = sdesc_sw128(ring + sq * C::kTileBytes, 16384, 1024);
-#pragma unroll
-            for (int step = 0; step < 2; ++step) {
-              if ((step == 0) == C::kDqFirst) {
-                if (kAtomicDq) {
-#pragma unroll
-                  for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4),
-                                id_q, kk > 0 ? 1u : 0u);
-                  mma_commit(&bar->dq_full);
-                }
-              } else {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                  const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                  if (C::kDsTmem)  // dS^T of query group kk at S^T column 16 kk + 8
-                    mma_bf16_ts(tDK, tS + kk * 16 + 8, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
-                                (it > 0 || kk > 0) ? 1u : 0u);
-                  else
-                    mma_bf16_ss(tDK, dsdesc_k + off, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
-                                (it > 0 || kk > 0) ? 1u : 0u);
-                }
-                // Q_i has been read by S^T (long complete) and dK: release its
-                // slot; the dS^T tile is free for the next elementwise step once
-                // dQ has read it as well (dq_free, which the next dP^T waits for)
-                mma_commit(&bar->ring_empty[sq]);
-                mma_commit(&bar->dk_done);
-              }
+            // (loops unrolled by 4: fully unrolled, the issuing warp's 72
+            // registers spill; not unrolled, a 32-cycle MMA at d = 64 outruns
+            // its issue)
+            if (kAtomicDq) {
+#pragma unroll 4
+              for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4), id_q,
+                            kk > 0 ? 1u : 0u);
+              mma_commit(&bar->dq_full);
             }
+            const uint64_t qdesc_mn = sdesc_sw128(ring + sq * C::kTileBytes, 16384, 1024);
+#pragma unroll 4
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+              mma_bf16_ss(tDK, dsdesc_k + off, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
+                          (it > 0 || kk > 0) ? 1u : 0u);
+            }
+            // Q_i has been read by S^T (long complete) and dK: release its slot;
+            // the dS^T tile is free for the next elementwise step (dQ, issued
+            // before dK, has read it too)
+            mma_commit(&bar->ring_empty[sq]);
+            mma_commit(&bar->dk_done);
           }
           // the item's dK and dV are complete, and its K and V read for the last time
           if (ok) mma_commit(&bar->acc_done);
@@ -572,7 +529,6 @@ __global__ void __launch_bounds__(512, 1)
       }
       __syncwarp();
     }
-    // warp 15 has no role
   } else if (warp >= 8) {
     // ------------------------------------------------------------------ reducers
     // (no role without the atomic dQ: the warpgroup keeps its launch budget)
@@ -650,8 +606,7 @@ __global__ void __launch_bounds__(512, 1)
     for (int item = blockIdx.x; alive && item < p.num_items; item += gridDim.x, ++w) {
       const BwdItem t = bwd_item<CAUSAL>(p, item);
       for (int it = 0; alive && it < t.n_it; ++it, ++g) {
-        const float* statL = reinterpret_cast<const float*>(sStatL + (g % C::kLEntries) * C::kStatRowBytes);
-        const float* statD = reinterpret_cast<const float*>(sStatD + (g % C::kDEntries) * C::kStatRowBytes);
+        const float* stat = reinterpret_cast<const float*>(sStat + (g % C::kStatEntries) * C::kStatBytes);
         // ---- phase 1: P^T = 2^(S^T c - L log2e) into TMEM, the fp32 values kept
         // in registers; issuer B starts dV as soon as all of P^T is written
         if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->s_full, g & 1, ctx, kSiteBwdS))) {
@@ -673,7 +628,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             // four queries' L*log2e (the same for every thread: a broadcast read)
-            const float4 l4 = *reinterpret_cast<const float4*>(statL + qc + 4 * e4);
+            const float4 l4 = *reinterpret_cast<const float4*>(stat + qc + 4 * e4);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int e = 4 * e4 + 2 * h;  // two queries at a time (packed fp32x2 arithmetic)
@@ -696,8 +651,7 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_before();
         mbar_arrive(&bar->p_done);
 
-        // ---- phase 2: dS^T = P^T o (dP^T - delta) into the shared dS^T tile
-        // (and, kDsTmem, beside P^T in TMEM, for dK),
+        // ---- phase 2: dS^T = P^T o (dP^T - delta) into the shared dS^T tile,
         // once the previous block's dK and dQ have read it (dP^T of this block
         // was issued after the reducers took the previous dQ out of TMEM; dK,
         // which runs after dQ, reports on its own)
@@ -718,7 +672,7 @@ __global__ void __launch_bounds__(512, 1)
           uint32_t dk[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(statD + qc + 4 * e4);
+            const float4 d4 = *reinterpret_cast<const float4*>(stat + 128 + qc + 4 * e4);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int e = 4 * e4 + 2 * h;
@@ -735,13 +689,8 @@ __global__ void __launch_bounds__(512, 1)
             *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
                 make_uint4(dk[4 * c16], dk[4 * c16 + 1], dk[4 * c16 + 2], dk[4 * c16 + 3]);
           }
-          if (C::kDsTmem) {  // beside P^T: columns qc + 8 and qc + 24 onwards, 8 each
-            tmem_st8(tS + qc + 8, dk);
-            tmem_st8(tS + qc + 24, dk + 8);
-          }
         }
         fence_async_shared();
-        if (C::kDsTmem) tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar->ew_done);
       }
