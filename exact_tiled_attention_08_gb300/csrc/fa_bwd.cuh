@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(256)
 // stores use.
 //
 // Warp roles (512 threads, four warpgroups; register budgets set with
-// setmaxnreg, 144 + 144 + 152 + 72 per thread = the launch's 128 x 4):
+// setmaxnreg, 136 + 136 + 152 + 88 per thread = the launch's 128 x 4):
 //   warps 0-7   elementwise: warpgroup g owns query columns [64 g, 64 g + 64)
 //               of dS
 //   warps 8-11  reducers: warp 8 + q takes TMEM lanes 32q.. (query rows) of
@@ -167,10 +167,10 @@ __global__ void __launch_bounds__(256)
 // warpgroups take kBwdWorkRegs, the reducers kBwdRedRegs (a reducer holds its
 // 32 rows of dQ_i, D values each, in registers), the issuing/producer
 // warpgroup keeps kBwdMiscRegs.  Each SM sub-partition holds one warp of
-// every warpgroup, so 2 x 144 + 152 + 72 = 512 = 4 x 128 uses exactly the
+// every warpgroup, so 2 x 136 + 152 + 88 = 512 = 4 x 128 uses exactly the
 // registers the block was launched with (128 per thread, which the host
 // checks before launching).
-constexpr uint32_t kBwdWorkRegs = 144, kBwdRedRegs = 152, kBwdMiscRegs = 72;
+constexpr uint32_t kBwdWorkRegs = 136, kBwdRedRegs = 152, kBwdMiscRegs = 88;
 static_assert(2 * kBwdWorkRegs + kBwdRedRegs + kBwdMiscRegs == 4 * 128, "register split must match the launch budget");
 
 // kAtomicDq: the kernel also forms dQ_i = dS K_j and adds it into the fp32
@@ -498,18 +498,18 @@ __global__ void __launch_bounds__(512, 1)
             // dS^T is written
             if (!(ok = wait_bounded_inl(&bar->ew_done, g & 1, ctx, kSiteBwdEw))) break;
             tc_fence_after();
-            // (loops unrolled by 4: fully unrolled, the issuing warp's 72
-            // registers spill; not unrolled, a 32-cycle MMA at d = 64 outruns
-            // its issue)
+            // (fully unrolled: the MMAs are issued back to back; in a loop, a
+            // 32-cycle MMA at d = 64 outruns its issue.  The issuing warps get
+            // 88 registers for the unrolled descriptors.)
             if (kAtomicDq) {
-#pragma unroll 4
+#pragma unroll
               for (int kk = 0; kk < 8; ++kk)
                 mma_bf16_ss(tDP, dsdesc_mn + (uint32_t)((kk * 2048) >> 4), kdesc_mn + (uint32_t)((kk * 2048) >> 4), id_q,
                             kk > 0 ? 1u : 0u);
               mma_commit(&bar->dq_full);
             }
             const uint64_t qdesc_mn = sdesc_sw128(ring + sq * C::kTileBytes, 16384, 1024);
-#pragma unroll 4
+#pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
               mma_bf16_ss(tDK, dsdesc_k + off, qdesc_mn + (uint32_t)((kk * 2048) >> 4), id_v,
