@@ -103,11 +103,14 @@ struct FwdCfg {
   static constexpr bool kSumByMma = FP8;
   static constexpr int kOCols = kSumByMma ? D + 16 : D;  // O accumulator columns
   static constexpr int kOnesBytes = FP8 ? 16 * 128 : 0;
-  // bf16 d = 128: O is normalised by the fp32 sum plus the rounding error of
-  // each key block's largest probability (see the softmax); bf16 d = 64, where
-  // the cheaper form gains nothing and raises register use, by the sum of the
-  // rounded probabilities themselves
-  static constexpr bool kBlockMaxCorr = !FP8 && D == 128;
+  // bf16: O is normalised by the fp32 sum plus the rounding error of each key
+  // block's largest probability (see the softmax)
+  static constexpr bool kBlockMaxCorr = !FP8;
+  // bf16 d = 64: the scores come out of TMEM in two halves, and the maximum of
+  // the first is taken while the second loads.  (Measured at d = 64 only
+  // together with kBlockMaxCorr there: either alone ran slower through the
+  // register allocation; at d = 128 it cost 3.6 % at N = 2048.)
+  static constexpr bool kSplitLoad = !FP8 && D == 64;
   // bf16 d = 64: a score buffer per tile (S_0 first, S_1 after the O
   // accumulators: 128 + 2 x 64 + 2 x 64 + 128 = 512 columns), so that a tile's
   // next scores never wait for the other tile to load its own.  At d = 128
@@ -482,10 +485,10 @@ __global__ void __launch_bounds__(352, 1)
       // FP8: the scores are the E4M3 products times the query and key block scales
       const float qsl2 = FP8 ? sl2 * __ldg(p.q_scale + (size_t)w.bh * p.nkb + (row_q0 >> 7)) : sl2;
       float m = -CUDART_INF_F;  // exponent reference (log2 units), a stale running max
-      // l: sum of the fp32 probabilities (for the LSE); lcorr (bf16, d = 128):
-      // the rounding errors of each key block's largest probability, so that
-      // l + lcorr normalises O (below); l_mma: the sum of the rounded
-      // probabilities (bf16 d = 64; FP8: formed by the tensor core)
+      // l: sum of the fp32 probabilities (for the LSE); lcorr (bf16): the
+      // rounding errors of each key block's largest probability, so that
+      // l + lcorr normalises O (below); l_mma: the normaliser (FP8: the sum of
+      // the rounded probabilities, formed by the tensor core)
       float l = 0.f, lcorr = 0.f, l_mma = 0.f;
       for (int j = 0; j < nb; ++j, ++uses) {
         // score factor of this key block (loaded before the wait hides its latency)
@@ -495,12 +498,43 @@ __global__ void __launch_bounds__(352, 1)
           break;
         }
         tc_fence_after();
+        // the maximum of 64 scores: a tree of 3-input maxima
+        auto max64 = [](const uint32_t* x, const uint32_t* y) {
+          float t1[22];
+#pragma unroll
+          for (int i = 0; i < 21; ++i) {
+            const int e = 3 * i;
+            t1[i] = max3(__uint_as_float(e < 32 ? x[e] : y[e - 32]), __uint_as_float(e + 1 < 32 ? x[e + 1] : y[e - 31]),
+                         __uint_as_float(e + 2 < 32 ? x[e + 2] : y[e - 30]));
+          }
+          t1[21] = __uint_as_float(y[31]);
+          float t2[8];
+#pragma unroll
+          for (int i = 0; i < 7; ++i) t2[i] = max3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
+          t2[7] = t1[21];
+          return max3(max3(t2[0], t2[1], t2[2]), max3(t2[3], t2[4], t2[5]), fmaxf(t2[6], t2[7]));
+        };
         uint32_t sr[4][32];
+        float mx_a = 0.f;  // kSplitLoad: the maximum of the first 64 scores, unmasked
+        if constexpr (C::kSplitLoad) {
+          tmem_ld32(tS, sr[0]);
+          tmem_ld32(tS + 32, sr[1]);
+          tmem_wait_ld();
+          reg_fence32(sr[0]);
+          reg_fence32(sr[1]);
+          tmem_ld32(tS + 64, sr[2]);
+          tmem_ld32(tS + 96, sr[3]);
+          mx_a = max64(sr[0], sr[1]);
+          tmem_wait_ld();
+          reg_fence32(sr[2]);
+          reg_fence32(sr[3]);
+        } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
-        tmem_wait_ld();
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
+          tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
+          for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
+        }
         // the scores are in registers: the next scores may now overwrite S
         tc_fence_before();
         mbar_arrive(&bar->s_free[C::kDualS ? t : 0]);
@@ -514,9 +548,12 @@ __global__ void __launch_bounds__(352, 1)
           for (int c = 0; c < 128; ++c)
             if (c > last) sr[c >> 5][c & 31] = __float_as_uint(-CUDART_INF_F);
         }
-        // row maximum as a tree of 3-input maxima
+        // row maximum as a tree of 3-input maxima (kSplitLoad: the two
+        // halves'; a masked block takes the first half again)
         float mx;
-        {
+        if constexpr (C::kSplitLoad) {
+          mx = fmaxf((tail || diag) ? max64(sr[0], sr[1]) : mx_a, max64(sr[2], sr[3]));
+        } else {
           float t1[43];
 #pragma unroll
           for (int i = 0; i < 42; ++i)
@@ -551,9 +588,9 @@ __global__ void __launch_bounds__(352, 1)
         // p = 2^(s c - m) two at a time, with their fp32 sum (four partial sums).
         const float2 c2 = make_float2(cj, cj);
         const float2 mneg2 = make_float2(-m, -m);
-        float2 acc[4], acc_mma[4];
+        float2 acc[4];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) acc[a] = acc_mma[a] = make_float2(0.f, 0.f);
+        for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
         if (C::kBlockMaxCorr) {
           // The P V product uses bf16-rounded probabilities.  O is normalised
           // by l plus the rounding error of each block's largest probability:
@@ -596,17 +633,10 @@ __global__ void __launch_bounds__(352, 1)
               pk[c][i] = pack_bf16x2(p0, p1);
             }
             acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
-            if (!C::kSumByMma && !C::kBlockMaxCorr)
-              acc_mma[i & 3] = __fadd2_rn(acc_mma[i & 3], make_float2(__uint_as_float(pk[c][i] << 16),
-                                                                     __uint_as_float(pk[c][i] & 0xffff0000u)));
           }
         }
         const float2 accs = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
         l = l * alpha + (accs.x + accs.y);
-        if (!C::kSumByMma && !C::kBlockMaxCorr) {
-          const float2 accm = __fadd2_rn(__fadd2_rn(acc_mma[0], acc_mma[1]), __fadd2_rn(acc_mma[2], acc_mma[3]));
-          l_mma = l_mma * alpha + (accm.x + accm.y);
-        }
         // P_t and O_t are in use until O_t += P_t(j-1) V_{j-1} has completed
         // (at j = 0 the previous item's epilogue has already waited for its
         // last product)
