@@ -564,20 +564,6 @@ __global__ void __launch_bounds__(512, 1)
         // before a tile is refilled, the reduce issued from it two chunks ago
         // must have read it.
         const int qrow0 = (t.i_start + it) * 128 + 32 * q;
-        // d = 128: the reduces of block g go out once the next block's dO tile
-        // has landed.  The SM's TMA unit serves both, and that load is on the
-        // path to the next dP^T, while the reduces have time to spare.
-        if (D == 128 && it + 1 < t.n_it) {
-          const int g1 = g + 1;
-          bool okw = true;
-          if (lane == 0)
-            okw = wait_bounded_inl(&bar->ring_full[C::kQSlots + g1 % C::kDoSlots], (g1 / C::kDoSlots) & 1, ctx,
-                                   kSiteBwdDq);
-          if (!__all_sync(0xffffffffu, __shfl_sync(0xffffffffu, okw, 0))) {
-            alive = false;
-            break;
-          }
-        }
 #pragma unroll
         for (int c = 0; c < kChunks; ++c, ++r) {
           uint8_t* tile = stage + (r & 1) * 4096;
