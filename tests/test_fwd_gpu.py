@@ -85,20 +85,27 @@ def test_forward_large_scale_forces_every_rescale():
     # row puts nearly all its weight on one or two keys.  The bound here is the
     # one bf16 arithmetic itself imposes, larger than the 1e-2 bar of the
     # standard workloads:
-    #  * P is rounded to bf16 before P V, |p^/p - 1| <= 2^-9, and O is divided
-    #    by the sum of the rounded p^, so each weight moves by at most
-    #    2^-8 w_k and O by at most 2^-8 max|V|;
+    #  * P is rounded to bf16 before P V, |p^/p - 1| <= 2^-9, and O's
+    #    normaliser (the fp32 sum plus the rounding error of each key block's
+    #    largest p) is within 2^-9 of the sum of the p^ that weight V, so each
+    #    weight moves by at most 2^-8 w_k and O by at most 2^-8 max|V|;
     #  * storing O in bf16 costs at most half an ulp, 2^-8 |O|;
     #  * plus 1e-3 for fp32 accumulation.
-    inp = make_inputs(1, 2, 1024, 128, seed=12)
-    o, lse = gpu_forward(inp, 1.0, False)
-    for h in range(2):
-        qn, kn, vn = (to_f32_numpy(inp[x][0, h]) for x in ("q", "k", "v"))
-        o_ref, l_ref = attention_fwd_ref(qn, kn, vn, 1.0, False)
-        err = np.abs(to_f32_numpy(o[0, h]) - o_ref)
-        bound = 2.0 ** -8 * (np.abs(vn).max() + np.abs(o_ref)) + 1e-3
-        assert (err <= bound).all(), (err - bound).max()
-        assert np.abs(lse[0, h].cpu().numpy() - l_ref).max() <= LSE_TOL
+    # The observed error is reported (and held to half the bound, where it has
+    # stayed: 0.35-0.36 of it at d = 128 and d = 64, causal or not).
+    for d in (128, 64):
+        for causal in (False, True):
+            inp = make_inputs(1, 2, 1024, d, seed=12)
+            o, lse = gpu_forward(inp, 1.0, causal)
+            for h in range(2):
+                qn, kn, vn = (to_f32_numpy(inp[x][0, h]) for x in ("q", "k", "v"))
+                o_ref, l_ref = attention_fwd_ref(qn, kn, vn, 1.0, causal)
+                err = np.abs(to_f32_numpy(o[0, h]) - o_ref)
+                bound = 2.0 ** -8 * (np.abs(vn).max() + np.abs(o_ref)) + 1e-3
+                ratio = float((err / bound).max())
+                print(f"d={d} causal={causal} head {h}: max |O - ref| {err.max():.3e}, {ratio:.3f} of the bound")
+                assert ratio <= 0.5, (d, causal, h, ratio)
+                assert np.abs(lse[0, h].cpu().numpy() - l_ref).max() <= LSE_TOL
 
 
 def test_equal_scores_give_mean_and_log_count():
