@@ -113,14 +113,17 @@ __global__ void __launch_bounds__(512)
     a[2] = b0 - b2;
     a[1] = b1 + b3;
     a[3] = b1 - b3;
-    // strides 4 .. 64: the partner element sits in lane ^ (stride / 4)
+    // strides 4 .. 64: the partner element sits in lane ^ (stride / 4); the
+    // lower element becomes a + o, the upper o - a, both as one fused
+    // multiply-add with the lane's sign (exact products, one rounding: the
+    // same values as the addition and the subtraction)
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) {
-      const bool upper = lane & m;
+      const float sgn_m = (lane & m) ? -1.f : 1.f;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const float o = __shfl_xor_sync(0xffffffffu, a[e], m);
-        a[e] = upper ? o - a[e] : a[e] + o;
+        a[e] = fmaf(a[e], sgn_m, o);
       }
     }
 #pragma unroll
