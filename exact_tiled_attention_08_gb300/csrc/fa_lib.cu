@@ -567,7 +567,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, const signed c
   if (ws_bytes < fa_fwd_fp8_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
     return FA_ERR_MISALIGNED;
-  // the operand preparation's grid has one y index per (batch, head)
+  // the V quantisation's grid has one y index per (batch, head)
   if ((long long)B * H > 65535) return FA_ERR_UNSUPPORTED;
   if ((st = check_device_ptrs({q, k, v, signs, o, lse, workspace})) != FA_OK) return st;
   const int BH = B * H;
@@ -583,20 +583,31 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, const signed c
   float* vs = reinterpret_cast<float*>(ws + w.vs);
   // 1. operands: rotate and quantise Q, K per block; V per channel, transposed
   const dim3 grid_rows((unsigned)nkb, (unsigned)BH);
-  const auto* qb = static_cast<const __nv_bfloat16*>(q);
-  const auto* kb = static_cast<const __nv_bfloat16*>(k);
   const auto* vb = static_cast<const __nv_bfloat16*>(v);
   const int8_t* sg = reinterpret_cast<const int8_t*>(signs);
   if (cudaMemsetAsync(vamax, 0, (size_t)BH * 128 * sizeof(unsigned), stream) != cudaSuccess) return FA_ERR_CUDA;
-  fa::fa_fp8_prepare_kernel<<<dim3((unsigned)nkb, (unsigned)BH, 3), 512, 0, stream>>>(qb, kb, vb, sg, q8, k8, qs, ks,
-                                                                                  vamax, N, nkb);
-  fa::fa_fp8_v_quant_kernel<<<grid_rows, 256, 0, stream>>>(vb, vamax, v8t, vs, N, nkb);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  // 2. attention on the E4M3 operands
+  CUtensorMap mxq, mxk, mxv;
+  if (!encode_bhnd(&mxq, q, BH, N, 128) || !encode_bhnd(&mxk, k, BH, N, 128) || !encode_bhnd(&mxv, v, BH, N, 128))
+    return FA_ERR_CUDA;
+  if (set_smem(fa::fa_fp8_prepare_kernel, fa::kFp8PrepSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return FA_ERR_CUDA;
+  const long long prep_items = 3LL * BH * nkb;
+  const long long prep_cap = (long long)sms * fa::kFp8PrepCtasPerSm;
+  // (a grid that is a multiple of 3 would give each CTA a single operand)
+  long long prep_grid = prep_items < prep_cap ? prep_items : prep_cap;
+  if (prep_grid > 1 && prep_grid % 3 == 0) --prep_grid;
   CUtensorMap mq, mk, mv;
   if (!encode_u8_3d(&mq, q8, 128, N, BH) || !encode_u8_3d(&mk, k8, 128, N, BH) ||
       !encode_u8_3d(&mv, v8t, 128, 128, (long long)BH * nkb))
     return FA_ERR_CUDA;
+  fa::fa_fp8_prepare_kernel<<<(unsigned)prep_grid, fa::kFp8PrepThreads, fa::kFp8PrepSmemBytes, stream>>>(
+      mxq, mxk, mxv, mq, mk, sg, qs, ks, vamax, N, nkb, BH, wait_limit_ns());
+  fa::fa_fp8_v_quant_kernel<<<grid_rows, 256, 0, stream>>>(vb, vamax, v8t, vs, N, nkb);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  // 2. attention on the E4M3 operands
   fa::FwdParams p{};
   p.o = static_cast<__nv_bfloat16*>(o);
   p.o_align32 = aligned32(o);
