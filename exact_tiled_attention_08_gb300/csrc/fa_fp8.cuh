@@ -28,8 +28,9 @@ constexpr float kE4m3Max = 448.f;
 
 // The preparation kernel: persistent CTAs of 128 threads, three per SM.  A
 // work item is one 128-row block of one operand of one (batch, head), item
-// 3 (bh nblk + blk) + op with op 0 = Q, 1 = K, 2 = V; CTA c takes items c,
-// c + G, c + 2 G, ... (G = the grid).  Every block arrives by TMA (two boxes
+// op (B H nblk) + bh nblk + blk with op 0 = Q, 1 = K, 2 = V; CTA c takes items
+// c, c + G, c + 2 G, ... (G = the grid), so that V comes last and is still in
+// L2 for its second pass.  Every block arrives by TMA (two boxes
 // of 64 channels x 128 rows, 128-byte swizzle, rows past N as zeros) into one
 // of two shared-memory buffers: the next item's block loads while the current
 // one is converted.  The E4M3 rows of a Q or K block go back into the buffer
@@ -181,10 +182,10 @@ __global__ void __launch_bounds__(kFp8PrepThreads, kFp8PrepCtasPerSm)
   float* red = reinterpret_cast<float*>(neg + 128);
   uint64_t* bar = reinterpret_cast<uint64_t*>(red + 4);  // [0], [1]: the two buffers
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 2);
-  const long long items = 3LL * BH * nblk;
+  const long long per_op = (long long)BH * nblk, items = 3 * per_op;
   auto load = [&](long long item, int b) {
-    const int op = (int)(item % 3);
-    const long long bb = item / 3;
+    const int op = item >= 2 * per_op ? 2 : (item >= per_op ? 1 : 0);
+    const long long bb = item - op * per_op;
     const int blk = (int)(bb % nblk), bh = (int)(bb / nblk);
     const CUtensorMap* map = op == 0 ? &map_q : (op == 1 ? &map_k : &map_v);
     mbar_arrive_expect_tx(&bar[b], kFp8PrepBufBytes);  // the whole box, zero rows included
@@ -212,8 +213,8 @@ __global__ void __launch_bounds__(kFp8PrepThreads, kFp8PrepCtasPerSm)
     }
     const bool ok = wait_bounded(&bar[k & 1], (k >> 1) & 1, ctx, kSiteFp8Prep);
     if (!__syncthreads_and(ok)) break;
-    const int op = (int)(item % 3);
-    const long long bb = item / 3;
+    const int op = item >= 2 * per_op ? 2 : (item >= per_op ? 1 : 0);
+    const long long bb = item - op * per_op;
     const int blk = (int)(bb % nblk), bh = (int)(bb / nblk);
     uint8_t* stage = buf + (k & 1) * kFp8PrepBufBytes;
     if (op == 2) {

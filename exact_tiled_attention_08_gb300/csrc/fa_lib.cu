@@ -596,9 +596,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, const signed c
     return FA_ERR_CUDA;
   const long long prep_items = 3LL * BH * nkb;
   const long long prep_cap = (long long)sms * fa::kFp8PrepCtasPerSm;
-  // (a grid that is a multiple of 3 would give each CTA a single operand)
-  long long prep_grid = prep_items < prep_cap ? prep_items : prep_cap;
-  if (prep_grid > 1 && prep_grid % 3 == 0) --prep_grid;
+  const long long prep_grid = prep_items < prep_cap ? prep_items : prep_cap;
   CUtensorMap mq, mk, mv;
   if (!encode_u8_3d(&mq, q8, 128, N, BH) || !encode_u8_3d(&mk, k8, 128, N, BH) ||
       !encode_u8_3d(&mv, v8t, 128, 128, (long long)BH * nkb))
