@@ -151,6 +151,33 @@ def test_fp8_quantised_operands_match_oracle(N, causal):
         assert within_one_quantum(v8t[h], want).all() and np.mean(v8t[h] == want) >= 0.995
 
 
+def test_fp8_quantised_operands_many_blocks_per_cta():
+    """3 operands x 32 heads x 17 blocks = 1632 blocks of 128 rows: more than
+    the preparation has CTAs, so each CTA walks several blocks through both of
+    its staging buffers and their barrier phases; N = 2148 leaves a ragged
+    last block in every head.  Every head's quantised Q, K and V against the
+    oracle, as above."""
+    B, H, N = 2, 16, 2148
+    inp = make_inputs(B, H, N, D, seed=505, with_dout=False)
+    signs = rotation_signs(D, 26)
+    _, _, ws = run_fp8(inp, signs, 1 / math.sqrt(D), False)
+    q8, k8, v8t, qs, ks, vs = decode_workspace(ws, B, H, N)
+    nkb = (N + 127) // 128
+    for bh in range(B * H):
+        b, h = divmod(bh, H)
+        for name, g8, gs in (("q", q8, qs), ("k", k8, ks)):
+            x8, sc = quantize_rows_per_block(to_f32_numpy(inp[name][b, h]), signs.numpy())
+            assert np.allclose(gs[bh], sc, rtol=1e-6, atol=0), (name, bh)
+            assert within_one_quantum(g8[bh], x8).all(), (name, bh)
+            assert np.mean(g8[bh] == x8) >= 0.995, (name, bh)
+        v8, sv = quantize_columns(to_f32_numpy(inp["v"][b, h]))
+        assert np.allclose(vs[bh], sv, rtol=1e-6, atol=0), bh
+        pad = np.zeros((nkb * 128, D))
+        pad[:N] = v8
+        want = pad.reshape(nkb, 128, D).transpose(0, 2, 1)
+        assert within_one_quantum(v8t[bh], want).all() and np.mean(v8t[bh] == want) >= 0.995, bh
+
+
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 17, 128, 129, 255, 300, 1000])
 def test_fp8_forward_small_and_ragged(N, causal):
