@@ -93,7 +93,8 @@ struct FwdCfg {
   static constexpr int kAtoms = D * kElemBytes / 128;             // 128-byte atom columns per tile
   static constexpr int kAtomElems = 128 / kElemBytes;             // elements per atom row
   static constexpr int kKSteps = D * kElemBytes / 32;             // MMAs of the S product (32 bytes of K each)
-  static constexpr int kThreads = 352;
+  static constexpr int kThreads = 384;  // 12 warps: three whole warpgroups (the register split)
+  static constexpr int kLaunchRegs = 168;  // 65536 / 384, rounded down to a multiple of 8
   static constexpr uint32_t kTmemCols = 512;
   // In FP8 the tensor core also forms the row sums of the rounded P that the
   // output product uses: V^T (read K-major) is followed by 16 rows of E4M3
@@ -226,11 +227,18 @@ __device__ __forceinline__ bool fwd_item(const FwdParams& p, int k, FwdItem& w) 
   return true;
 }
 
+// Register budgets per thread after setmaxnreg: each SM sub-partition holds
+// one warp of every warpgroup, so 2 x 208 + 88 = 504 = 3 x 168 uses exactly
+// the registers the block was launched with (168 per thread, which the host
+// checks before launching).
+constexpr uint32_t kFwdSoftRegs = 208, kFwdMiscRegs = 88;
+static_assert(2 * kFwdSoftRegs + kFwdMiscRegs == 3 * 168, "register split must match the launch budget");
+
 // SOFT_EXP: of every four pairs of probabilities a softmax thread forms, the
 // first SOFT_EXP pairs take ex2_cubic on the FMA pipe and the rest the MUFU's
 // ex2.approx (0: all on the MUFU).
 template <int D, bool CAUSAL, bool FP8 = false, int SOFT_EXP = 0>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
   using C = FwdCfg<D, FP8>;
@@ -290,181 +298,189 @@ __global__ void __launch_bounds__(352, 1)
   // Every role walks the same sequence of items; the ring fills, the uses of
   // S and the per-tile products are counted across items, so barrier phases
   // carry over from one item to the next.
-  if (warp == 9) {
-    // ------------------------------------------------------------------ TMA producer
-    // fill order = consumption order: K_0, V_0, K_1, V_1, ... of each item in turn
-    if (lane == 0) {
-      int fill = 0, nq = 0;
-      bool ok = true;
-      auto load_kv = [&](int j, int kv, int bh) -> bool {
-        const int s = fill % C::kSlots;
-        const uint32_t u = fill / C::kSlots;
-        if (!wait_bounded(&bar->kv_empty[s], (u & 1) ^ 1, ctx, kSiteFwdProducer)) return false;
-        mbar_arrive_expect_tx(&bar->kv_full[s], C::kTileBytes);
-        if (FP8 && kv) {
-          // V^T of key block j: d rows of 128 keys, tile (bh, j) of the transposed layout
-          tma_load_3d(sKV + C::slot_offset(s), &map_v, &bar->kv_full[s], 0, 0, bh * p.nkb + j);
-        } else {
-          const CUtensorMap* map = kv ? &map_v : &map_k;
-          for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_3d(sKV + C::slot_offset(s) + a * 16384, map, &bar->kv_full[s], a * C::kAtomElems, j * 128, bh);
-        }
-        ++fill;
-        return true;
-      };
-      FwdItem w;
-      for (int k = 0; ok && fwd_item<CAUSAL>(p, k, w); ++k) {
-        const int nb_max = max(w.nb0, w.nb1);
-        if (nb_max == 0) continue;  // a single tile past N
-        const bool has1 = w.nb1 > 0;
-        // the first key/value block needs only ring slots: it goes out
-        // before Q, whose buffer the previous item may still be reading
-        ok = load_kv(0, 0, w.bh) && load_kv(0, 1, w.bh);
-        if (ok && nq > 0) ok = wait_bounded(&bar->q_empty, (nq - 1) & 1, ctx, kSiteFwdQEmpty);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bar->q_full, C::kTileBytes * (has1 ? 2 : 1));
-        for (int t = 0; t < (has1 ? 2 : 1); ++t)
-          for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &map_q, &bar->q_full, a * C::kAtomElems, w.q0 + 128 * t,
-                        w.bh);
-        ++nq;
-        // the next item's queries go to L2 now, so that their load at the
-        // item boundary is served from there
-        FwdItem nx;
-        if (fwd_item<CAUSAL>(p, k + 1, nx) && nx.nb0 > 0)
-          for (int t = 0; t < (nx.nb1 > 0 ? 2 : 1); ++t)
+  // Register split: the issuing and producer warpgroup (warps 8-11; warp 11
+  // has no role and is there to make the warpgroup whole) gives registers
+  // back down to kFwdMiscRegs a thread, the two softmax warpgroups take
+  // kFwdSoftRegs.
+  if (warp >= 8) {
+    setmaxnreg_dec<kFwdMiscRegs>();
+    if (warp == 9) {
+      // ------------------------------------------------------------------ TMA producer
+      // fill order = consumption order: K_0, V_0, K_1, V_1, ... of each item in turn
+      if (lane == 0) {
+        int fill = 0, nq = 0;
+        bool ok = true;
+        auto load_kv = [&](int j, int kv, int bh) -> bool {
+          const int s = fill % C::kSlots;
+          const uint32_t u = fill / C::kSlots;
+          if (!wait_bounded_inl(&bar->kv_empty[s], (u & 1) ^ 1, ctx, kSiteFwdProducer)) return false;
+          mbar_arrive_expect_tx(&bar->kv_full[s], C::kTileBytes);
+          if (FP8 && kv) {
+            // V^T of key block j: d rows of 128 keys, tile (bh, j) of the transposed layout
+            tma_load_3d(sKV + C::slot_offset(s), &map_v, &bar->kv_full[s], 0, 0, bh * p.nkb + j);
+          } else {
+            const CUtensorMap* map = kv ? &map_v : &map_k;
             for (int a = 0; a < C::kAtoms; ++a)
-              tma_prefetch_l2_3d(&map_q, a * C::kAtomElems, nx.q0 + 128 * t, nx.bh);
-        for (int j = 1; ok && j < nb_max; ++j) ok = load_kv(j, 0, w.bh) && load_kv(j, 1, w.bh);
-      }
-      // every copy this thread started must land before the CTA can exit
-      if (nq > 0) wait_drain(&bar->q_full, (nq - 1) & 1, kDrainLimitNs);
-      for (int s = 0; s < C::kSlots; ++s) {
-        if (fill > s) {
-          const int uses = (fill - 1 - s) / C::kSlots + 1;
-          wait_drain(&bar->kv_full[s], (uses - 1) & 1, kDrainLimitNs);
+              tma_load_3d(sKV + C::slot_offset(s) + a * 16384, map, &bar->kv_full[s], a * C::kAtomElems, j * 128, bh);
+          }
+          ++fill;
+          return true;
+        };
+        FwdItem w;
+        for (int k = 0; ok && fwd_item<CAUSAL>(p, k, w); ++k) {
+          const int nb_max = max(w.nb0, w.nb1);
+          if (nb_max == 0) continue;  // a single tile past N
+          const bool has1 = w.nb1 > 0;
+          // the first key/value block needs only ring slots: it goes out
+          // before Q, whose buffer the previous item may still be reading
+          ok = load_kv(0, 0, w.bh) && load_kv(0, 1, w.bh);
+          if (ok && nq > 0) ok = wait_bounded_inl(&bar->q_empty, (nq - 1) & 1, ctx, kSiteFwdQEmpty);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bar->q_full, C::kTileBytes * (has1 ? 2 : 1));
+          for (int t = 0; t < (has1 ? 2 : 1); ++t)
+            for (int a = 0; a < C::kAtoms; ++a)
+              tma_load_3d(sQ + t * C::kTileBytes + a * 16384, &map_q, &bar->q_full, a * C::kAtomElems, w.q0 + 128 * t,
+                          w.bh);
+          ++nq;
+          // the next item's queries go to L2 now, so that their load at the
+          // item boundary is served from there
+          FwdItem nx;
+          if (fwd_item<CAUSAL>(p, k + 1, nx) && nx.nb0 > 0)
+            for (int t = 0; t < (nx.nb1 > 0 ? 2 : 1); ++t)
+              for (int a = 0; a < C::kAtoms; ++a)
+                tma_prefetch_l2_3d(&map_q, a * C::kAtomElems, nx.q0 + 128 * t, nx.bh);
+          for (int j = 1; ok && j < nb_max; ++j) ok = load_kv(j, 0, w.bh) && load_kv(j, 1, w.bh);
+        }
+        // every copy this thread started must land before the CTA can exit
+        if (nq > 0) wait_drain_inl(&bar->q_full, (nq - 1) & 1, kDrainLimitNs);
+        for (int s = 0; s < C::kSlots; ++s) {
+          if (fill > s) {
+            const int uses = (fill - 1 - s) / C::kSlots + 1;
+            wait_drain_inl(&bar->kv_full[s], (uses - 1) & 1, kDrainLimitNs);
+          }
         }
       }
-    }
-    __syncwarp();
-  } else if (warp == 8) {
-    // ------------------------------------------------------------------ S issuer
-    // K_j is ring fill 2g (g counts key blocks over all items); S(k) waits
-    // until the tile that used S before has loaded it
-    if (lane == 0) {
-      const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
-      const uint64_t qdesc0 = sdesc_sw128(sq, 16, 1024);
-      const uint64_t qdesc1 = sdesc_sw128(sq + C::kTileBytes, 16, 1024);
-      constexpr uint32_t id_s = FP8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
-      int s_uses[2] = {0, 0}, g = 0, nq = 0;  // S products issued into each score buffer
-      bool ok = !(p.debug_stall && !wait_bounded(&bar->never, 0, ctx, kSiteStall));
-      FwdItem w;
-      for (int k = 0; ok && fwd_item<CAUSAL>(p, k, w); ++k) {
-        const int nb_max = max(w.nb0, w.nb1);
-        if (nb_max == 0) continue;
-        if (!wait_bounded(&bar->q_full, nq & 1, ctx, kSiteFwdQ)) break;
-        ++nq;
-        for (int j = 0; ok && j < nb_max; ++j, ++g) {
-          const int f = 2 * g;
-          const int ks = f % C::kSlots;
-          if (!wait_bounded(&bar->kv_full[ks], (f / C::kSlots) & 1, ctx, kSiteFwdK)) {
-            ok = false;
-            break;
-          }
-          const uint64_t kdesc = sdesc_sw128(skv + C::slot_offset(ks), 16, 1024);
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (j < (t ? w.nb1 : w.nb0)) {
-              const int sb = C::kDualS ? t : 0;
-              if (s_uses[sb] > 0 && !wait_bounded(&bar->s_free[sb], (s_uses[sb] - 1) & 1, ctx, kSiteFwdSFree)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint64_t qd = t ? qdesc1 : qdesc0;
-#pragma unroll
-              for (int kk = 0; kk < C::kKSteps; ++kk) {
-                const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                const uint32_t scol = tmem + (sb ? C::kSCol1 : C::kSCol);
-                if constexpr (FP8)
-                  mma_e4m3_ss(scol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
-                else
-                  mma_bf16_ss(scol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(&bar->s_full[t]);
-              ++s_uses[sb];
+      __syncwarp();
+    } else if (warp == 8) {
+      // ------------------------------------------------------------------ S issuer
+      // K_j is ring fill 2g (g counts key blocks over all items); S(k) waits
+      // until the tile that used S before has loaded it
+      if (lane == 0) {
+        const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
+        const uint64_t qdesc0 = sdesc_sw128(sq, 16, 1024);
+        const uint64_t qdesc1 = sdesc_sw128(sq + C::kTileBytes, 16, 1024);
+        constexpr uint32_t id_s = FP8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
+        int s_uses[2] = {0, 0}, g = 0, nq = 0;  // S products issued into each score buffer
+        bool ok = !(p.debug_stall && !wait_bounded_inl(&bar->never, 0, ctx, kSiteStall));
+        FwdItem w;
+        for (int k = 0; ok && fwd_item<CAUSAL>(p, k, w); ++k) {
+          const int nb_max = max(w.nb0, w.nb1);
+          if (nb_max == 0) continue;
+          if (!wait_bounded_inl(&bar->q_full, nq & 1, ctx, kSiteFwdQ)) break;
+          ++nq;
+          for (int j = 0; ok && j < nb_max; ++j, ++g) {
+            const int f = 2 * g;
+            const int ks = f % C::kSlots;
+            if (!wait_bounded_inl(&bar->kv_full[ks], (f / C::kSlots) & 1, ctx, kSiteFwdK)) {
+              ok = false;
+              break;
             }
+            const uint64_t kdesc = sdesc_sw128(skv + C::slot_offset(ks), 16, 1024);
+  #pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (j < (t ? w.nb1 : w.nb0)) {
+                const int sb = C::kDualS ? t : 0;
+                if (s_uses[sb] > 0 && !wait_bounded_inl(&bar->s_free[sb], (s_uses[sb] - 1) & 1, ctx, kSiteFwdSFree)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint64_t qd = t ? qdesc1 : qdesc0;
+  #pragma unroll
+                for (int kk = 0; kk < C::kKSteps; ++kk) {
+                  const uint32_t off = (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                  const uint32_t scol = tmem + (sb ? C::kSCol1 : C::kSCol);
+                  if constexpr (FP8)
+                    mma_e4m3_ss(scol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
+                  else
+                    mma_bf16_ss(scol, qd + off, kdesc + off, id_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar->s_full[t]);
+                ++s_uses[sb];
+              }
+            }
+            if (!ok) break;
+            mma_commit(&bar->kv_empty[ks]);
           }
           if (!ok) break;
-          mma_commit(&bar->kv_empty[ks]);
+          // the item's queries have been read: their buffer may take the next item's
+          mma_commit(&bar->q_empty);
         }
-        if (!ok) break;
-        // the item's queries have been read: their buffer may take the next item's
-        mma_commit(&bar->q_empty);
+        // everything issued must complete before the tensor memory is released
+        mma_commit(&bar->drain[0]);
+        wait_drain_inl(&bar->drain[0], 0, kDrainLimitNs);
       }
-      // everything issued must complete before the tensor memory is released
-      mma_commit(&bar->drain[0]);
-      wait_drain(&bar->drain[0], 0, kDrainLimitNs);
-    }
-    __syncwarp();
-  } else if (warp == 10) {
-    // ------------------------------------------------------------------ P V issuer
-    // V_j is ring fill 2g+1; O_t += P_t(j) V_j once the softmax of tile t wrote P_t(j)
-    if (lane == 0) {
-      const uint32_t skv = smem_u32(sKV);
-      // bf16: V read N-major; FP8: V^T read K-major (with the ones rows after it)
-      constexpr uint32_t id_pv = FP8 ? idesc_e4m3_f32(128, C::kOCols) : idesc_bf16_f32(128, C::kOCols, false, true);
-      int g = 0;
-      int pv_uses[2] = {0, 0};
-      bool ok = true;
-      FwdItem w;
-      for (int k = 0; ok && fwd_item<CAUSAL>(p, k, w); ++k) {
-        const int nb_max = max(w.nb0, w.nb1);
-        if (nb_max == 0) continue;
-        for (int j = 0; ok && j < nb_max; ++j, ++g) {
-          const int f = 2 * g + 1;
-          const int vs = f % C::kSlots;
-          if (!wait_bounded(&bar->kv_full[vs], (f / C::kSlots) & 1, ctx, kSiteFwdV)) {
-            ok = false;
-            break;
-          }
-          // (FP8: the ones rows after V^T make the last 16 columns of O the row sums)
-          const uint64_t vdesc = sdesc_sw128(skv + C::slot_offset(vs), FP8 ? 16 : 16384, 1024);
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (j < (t ? w.nb1 : w.nb0)) {
-              if (!wait_bounded(&bar->p_full[t], pv_uses[t] & 1, ctx, kSiteFwdP)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint32_t dcol = tmem + (t ? C::kOCol1 : C::kOCol0);
-              const uint32_t pcol = tmem + (t ? C::kPCol1 : C::kPCol0);
-              if constexpr (FP8) {
-                // 4 steps of 32 keys: P from 8 TMEM columns each, V^T rows at +32 bytes
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  mma_e4m3_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 32) >> 4), id_pv,
-                              (j > 0 || kk > 0) ? 1u : 0u);
-              } else {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                  mma_bf16_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 2048) >> 4), id_pv,
-                              (j > 0 || kk > 0) ? 1u : 0u);
-              }
-              mma_commit(&bar->pv_done[t]);
-              ++pv_uses[t];
+      __syncwarp();
+    } else if (warp == 10) {
+      // ------------------------------------------------------------------ P V issuer
+      // V_j is ring fill 2g+1; O_t += P_t(j) V_j once the softmax of tile t wrote P_t(j)
+      if (lane == 0) {
+        const uint32_t skv = smem_u32(sKV);
+        // bf16: V read N-major; FP8: V^T read K-major (with the ones rows after it)
+        constexpr uint32_t id_pv = FP8 ? idesc_e4m3_f32(128, C::kOCols) : idesc_bf16_f32(128, C::kOCols, false, true);
+        int g = 0;
+        int pv_uses[2] = {0, 0};
+        bool ok = true;
+        FwdItem w;
+        for (int k = 0; ok && fwd_item<CAUSAL>(p, k, w); ++k) {
+          const int nb_max = max(w.nb0, w.nb1);
+          if (nb_max == 0) continue;
+          for (int j = 0; ok && j < nb_max; ++j, ++g) {
+            const int f = 2 * g + 1;
+            const int vs = f % C::kSlots;
+            if (!wait_bounded_inl(&bar->kv_full[vs], (f / C::kSlots) & 1, ctx, kSiteFwdV)) {
+              ok = false;
+              break;
             }
+            // (FP8: the ones rows after V^T make the last 16 columns of O the row sums)
+            const uint64_t vdesc = sdesc_sw128(skv + C::slot_offset(vs), FP8 ? 16 : 16384, 1024);
+  #pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (j < (t ? w.nb1 : w.nb0)) {
+                if (!wait_bounded_inl(&bar->p_full[t], pv_uses[t] & 1, ctx, kSiteFwdP)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint32_t dcol = tmem + (t ? C::kOCol1 : C::kOCol0);
+                const uint32_t pcol = tmem + (t ? C::kPCol1 : C::kPCol0);
+                if constexpr (FP8) {
+                  // 4 steps of 32 keys: P from 8 TMEM columns each, V^T rows at +32 bytes
+  #pragma unroll
+                  for (int kk = 0; kk < 4; ++kk)
+                    mma_e4m3_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 32) >> 4), id_pv,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                } else {
+  #pragma unroll
+                  for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ts(dcol, pcol + kk * 8, vdesc + (uint32_t)((kk * 2048) >> 4), id_pv,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&bar->pv_done[t]);
+                ++pv_uses[t];
+              }
+            }
+            if (!ok) break;
+            mma_commit(&bar->kv_empty[vs]);
           }
-          if (!ok) break;
-          mma_commit(&bar->kv_empty[vs]);
         }
+        mma_commit(&bar->drain[1]);
+        wait_drain_inl(&bar->drain[1], 0, kDrainLimitNs);
       }
-      mma_commit(&bar->drain[1]);
-      wait_drain(&bar->drain[1], 0, kDrainLimitNs);
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    setmaxnreg_inc<kFwdSoftRegs>();
     // ------------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2;
     const int wq = warp & 3;
@@ -493,7 +509,7 @@ __global__ void __launch_bounds__(352, 1)
       for (int j = 0; j < nb; ++j, ++uses) {
         // score factor of this key block (loaded before the wait hides its latency)
         const float cj = FP8 ? qsl2 * __ldg(p.k_scale + (size_t)w.bh * p.nkb + j) : sl2;
-        if (!__all_sync(0xffffffffu, wait_bounded(&bar->s_full[t], uses & 1, ctx, kSiteFwdS))) {
+        if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->s_full[t], uses & 1, ctx, kSiteFwdS))) {
           alive = false;
           break;
         }
@@ -641,7 +657,7 @@ __global__ void __launch_bounds__(352, 1)
         // (at j = 0 the previous item's epilogue has already waited for its
         // last product)
         if (j > 0) {
-          if (!__all_sync(0xffffffffu, wait_bounded(&bar->pv_done[t], (uses - 1) & 1, ctx, kSiteFwdPvDone))) {
+          if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->pv_done[t], (uses - 1) & 1, ctx, kSiteFwdPvDone))) {
             alive = false;
             break;
           }
@@ -687,7 +703,7 @@ __global__ void __launch_bounds__(352, 1)
       // Once the tensor memory loads below have completed, the next item's
       // first P V product may overwrite O_t (it is issued only after this
       // warpgroup has written the next P_t).
-      if (!__all_sync(0xffffffffu, wait_bounded(&bar->pv_done[t], (uses - 1) & 1, ctx, kSiteFwdO))) {
+      if (!__all_sync(0xffffffffu, wait_bounded_inl(&bar->pv_done[t], (uses - 1) & 1, ctx, kSiteFwdO))) {
         alive = false;
         break;
       }

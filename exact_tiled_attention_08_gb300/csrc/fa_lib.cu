@@ -147,6 +147,10 @@ fa_status launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   using C = fa::FwdCfg<D, FP8>;
   auto kernel = fa::fa_fwd_kernel<D, CAUSAL, FP8, SOFT_EXP>;
   if (set_smem(kernel, C::kSmemBytes) != cudaSuccess) return FA_ERR_CUDA;
+  // the warpgroups re-divide the block's registers (setmaxnreg); that only
+  // works if the block really gets kLaunchRegs per thread
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess || attr.numRegs != C::kLaunchRegs) return FA_ERR_CUDA;
   // persistent CTAs: one per SM (the kernel holds a whole SM), never more than there are items
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
