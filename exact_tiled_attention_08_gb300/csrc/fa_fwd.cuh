@@ -95,6 +95,15 @@ struct FwdCfg {
   static constexpr int kKSteps = D * kElemBytes / 32;             // MMAs of the S product (32 bytes of K each)
   static constexpr int kThreads = 384;  // 12 warps: three whole warpgroups (the register split)
   static constexpr int kLaunchRegs = 168;  // 65536 / 384, rounded down to a multiple of 8
+  // Register budgets per thread after setmaxnreg: each SM sub-partition holds
+  // one warp of every warpgroup, so 2 kSoftRegs + kMiscRegs = 3 x 168 uses
+  // exactly the registers the block was launched with (168 per thread, which
+  // the host checks before launching).  Measured: 216 for the softmax warps
+  // at d = 64 (+7 %) and in FP8, 208 for bf16 at d = 128 (216 lost 1 % there).
+  static constexpr uint32_t kSoftRegs = (D == 64 || FP8) ? 216 : 208;
+  static constexpr uint32_t kMiscRegs = 3 * kLaunchRegs - 2 * kSoftRegs;
+  static_assert(kSoftRegs % 8 == 0 && kSoftRegs <= 256 && kMiscRegs % 8 == 0 && kMiscRegs >= 24,
+                "setmaxnreg takes multiples of 8 in [24, 256]");
   static constexpr uint32_t kTmemCols = 512;
   // In FP8 the tensor core also forms the row sums of the rounded P that the
   // output product uses: V^T (read K-major) is followed by 16 rows of E4M3
@@ -227,12 +236,6 @@ __device__ __forceinline__ bool fwd_item(const FwdParams& p, int k, FwdItem& w) 
   return true;
 }
 
-// Register budgets per thread after setmaxnreg: each SM sub-partition holds
-// one warp of every warpgroup, so 2 x 208 + 88 = 504 = 3 x 168 uses exactly
-// the registers the block was launched with (168 per thread, which the host
-// checks before launching).
-constexpr uint32_t kFwdSoftRegs = 208, kFwdMiscRegs = 88;
-static_assert(2 * kFwdSoftRegs + kFwdMiscRegs == 3 * 168, "register split must match the launch budget");
 
 // SOFT_EXP: of every four pairs of probabilities a softmax thread forms, the
 // first SOFT_EXP pairs take ex2_cubic on the FMA pipe and the rest the MUFU's
@@ -300,10 +303,10 @@ __global__ void __launch_bounds__(384, 1)
   // carry over from one item to the next.
   // Register split: the issuing and producer warpgroup (warps 8-11; warp 11
   // has no role and is there to make the warpgroup whole) gives registers
-  // back down to kFwdMiscRegs a thread, the two softmax warpgroups take
-  // kFwdSoftRegs.
+  // back down to C::kMiscRegs a thread, the two softmax warpgroups take
+  // C::kSoftRegs.
   if (warp >= 8) {
-    setmaxnreg_dec<kFwdMiscRegs>();
+    setmaxnreg_dec<C::kMiscRegs>();
     if (warp == 9) {
       // ------------------------------------------------------------------ TMA producer
       // fill order = consumption order: K_0, V_0, K_1, V_1, ... of each item in turn
@@ -480,7 +483,7 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
     }
   } else {
-    setmaxnreg_inc<kFwdSoftRegs>();
+    setmaxnreg_inc<C::kSoftRegs>();
     // ------------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2;
     const int wq = warp & 3;
