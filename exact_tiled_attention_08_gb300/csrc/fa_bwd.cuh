@@ -164,14 +164,28 @@ __global__ void __launch_bounds__(256)
 // dQ_i goes into the dP^T columns once the elementwise step has read them.
 // ---------------------------------------------------------------------------
 // Register budgets per thread after setmaxnreg: the two elementwise
-// warpgroups take kBwdWorkRegs, the reducers kBwdRedRegs (a reducer holds its
+// warpgroups take BwdRegs::kWork, the reducers kRed (a reducer holds its
 // 32 rows of dQ_i, D values each, in registers), the issuing/producer
-// warpgroup keeps kBwdMiscRegs.  Each SM sub-partition holds one warp of
+// warpgroup keeps kMisc.  Each SM sub-partition holds one warp of
 // every warpgroup, so 2 x 136 + 152 + 88 = 512 = 4 x 128 uses exactly the
 // registers the block was launched with (128 per thread, which the host
 // checks before launching).
-constexpr uint32_t kBwdWorkRegs = 136, kBwdRedRegs = 152, kBwdMiscRegs = 88;
-static_assert(2 * kBwdWorkRegs + kBwdRedRegs + kBwdMiscRegs == 4 * 128, "register split must match the launch budget");
+// At d = 64 a reducer's rows are half as long, and the elementwise warps,
+// which set the pace there, take 160 (2 x 160 + 104 + 88 = 512; the reducers
+// then give registers back).  Without the atomic dQ the reducer warpgroup
+// has no role and keeps the launch budget (2 x 136 + 128 + 88 < 512).
+// setmaxnreg.inc only raises a warp's count and .dec only lowers it.
+template <int D, bool kAtomicDq>
+struct BwdRegs {
+  static constexpr uint32_t kLaunch = 128, kMisc = 88;
+  static constexpr uint32_t kWork = (D == 64 && kAtomicDq) ? 160 : 136;
+  static constexpr uint32_t kRed = kAtomicDq ? 4 * kLaunch - 2 * kWork - kMisc : kLaunch;
+  static_assert(2 * kWork + kRed + kMisc <= 4 * kLaunch, "register split must fit the launch budget");
+  static_assert(kWork > kLaunch && kMisc < kLaunch, "the elementwise warps raise, the issuing warps lower");
+  static_assert(kWork % 8 == 0 && kWork <= 256 && kRed % 8 == 0 && kRed >= 24 && kRed <= 256 && kMisc % 8 == 0 &&
+                    kMisc >= 24,
+                "setmaxnreg takes multiples of 8 in [24, 256]");
+};
 
 // kAtomicDq: the kernel also forms dQ_i = dS K_j and adds it into the fp32
 // accumulator (reducer warps); otherwise dQ is left to the separate
@@ -278,6 +292,7 @@ __global__ void __launch_bounds__(512, 1)
                   const __grid_constant__ CUtensorMap map_lse2, const __grid_constant__ CUtensorMap map_delta,
                   const __grid_constant__ CUtensorMap map_dq, const BwdParams p) {
   using C = BwdCfg<D, kAtomicDq>;
+  static_assert(BwdRegs<D, kAtomicDq>::kLaunch == C::kLaunchRegs, "register split of the launch budget");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {
     // the 128-byte-swizzled tiles need 1024-byte alignment: report, do nothing
@@ -337,7 +352,7 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t tmem = bar->tmem_base;
   const WaitCtx ctx{&bar->abort_flag, p.wait_limit_ns};
   if (warp >= 12) {
-    setmaxnreg_dec<kBwdMiscRegs>();
+    setmaxnreg_dec<BwdRegs<D, kAtomicDq>::kMisc>();
     if (warp == 13 || warp == 15) {
       // ---------------------------------------------------------------- TMA producers
       // warp 13: K and V of each item and the Q tiles (with the statistics),
@@ -533,7 +548,11 @@ __global__ void __launch_bounds__(512, 1)
     // ------------------------------------------------------------------ reducers
     // (no role without the atomic dQ: the warpgroup keeps its launch budget)
     if (kAtomicDq) {
-    setmaxnreg_inc<kBwdRedRegs>();
+    using R = BwdRegs<D, kAtomicDq>;
+    if constexpr (R::kRed > R::kLaunch)
+      setmaxnreg_inc<R::kRed>();
+    else if constexpr (R::kRed < R::kLaunch)
+      setmaxnreg_dec<R::kRed>();
     const int q = warp & 3;
     const uint32_t tDQ = tmem + C::kDpCol + ((uint32_t)(q * 32) << 16);
     uint8_t* stage = sStage + q * 8192;  // two 4 KB tiles
@@ -592,7 +611,7 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else {
     // ------------------------------------------------------------------ elementwise
-    setmaxnreg_inc<kBwdWorkRegs>();
+    setmaxnreg_inc<BwdRegs<D, kAtomicDq>::kWork>();
     const int grp = warp >> 2;  // warpgroup: query columns [64 grp, 64 grp + 64)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row

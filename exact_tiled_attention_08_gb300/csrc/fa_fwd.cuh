@@ -104,6 +104,7 @@ struct FwdCfg {
   static constexpr uint32_t kMiscRegs = 3 * kLaunchRegs - 2 * kSoftRegs;
   static_assert(kSoftRegs % 8 == 0 && kSoftRegs <= 256 && kMiscRegs % 8 == 0 && kMiscRegs >= 24,
                 "setmaxnreg takes multiples of 8 in [24, 256]");
+  static_assert(kSoftRegs > kLaunchRegs && kMiscRegs < kLaunchRegs, "setmaxnreg.inc raises, .dec lowers");
   static constexpr uint32_t kTmemCols = 512;
   // In FP8 the tensor core also forms the row sums of the rounded P that the
   // output product uses: V^T (read K-major) is followed by 16 rows of E4M3
