@@ -14,12 +14,14 @@
 // sequence of items (fwd_item below), and the roles run on from one item to
 // the next without draining, so the next pair's queries load while the
 // tensor core finishes the current pair and its epilogue overlaps the next
-// pair's first score products.  Warp roles (352 threads):
+// pair's first score products.  Warp roles (384 threads):
 //   warps 0-3  softmax warpgroup of tile 0 (thread = query row)
 //   warps 4-7  softmax warpgroup of tile 1
 //   warp  8    issues the score products S = Q K^T (one thread); TMEM owner
 //   warp  9    TMA producer (one thread)
 //   warp  10   issues the output products O += P V (one thread)
+//   warp  11   no role: it completes the third warpgroup, whose registers
+//              (setmaxnreg) go to the softmax warpgroups
 // The MMA queue of an SM is shallow: a thread that waits or keeps books
 // between groups of MMAs leaves the tensor core idle, so the two kinds of
 // product are issued by two threads whose waits overlap each other's MMAs.
