@@ -149,8 +149,22 @@ def test_fwd_fp8_validation(lib):
     assert call(ws=BAD) == fa.FA_ERR_MISALIGNED
 
 
+@pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 2, 129), (4, 16, 2048), (1, 8, 32768)])
+def test_fwd_fp8_workspace_bytes_follow_the_documented_layout(lib, B, H, N):
+    # Q R, K R [B][H][N][128] E4M3; V^T [B][H][nkb][128][128] E4M3; query and key
+    # block scales [B][H][nkb] fp32; channel maxima and scales [B][H][128] fp32;
+    # each part on a 256-byte boundary
+    bh, nkb = B * H, (N + 127) // 128
+
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    want = 2 * up(bh * N * 128) + up(bh * nkb * 128 * 128) + 2 * up(bh * nkb * 4) + 2 * up(bh * 128 * 4)
+    assert lib.fa_fwd_fp8_workspace_bytes(B, H, N, 128) == want
+
+
 def test_fwd_fp8_rejects_more_than_65535_heads(lib):
-    # the operand preparation's grid has one y index per (batch, head)
+    # the V quantisation's grid has one y index per (batch, head)
     B, H, N = 256, 257, 128
     need = lib.fa_fwd_fp8_workspace_bytes(B, H, N, 128)
     assert need > 0
